@@ -1,0 +1,154 @@
+"""Seeded synthetic inputs for the Llama-3 8B grouped-query attention block.
+
+This module only draws numbers: it holds none of the block's arithmetic, so both the
+CUDA path and the fp64 oracle can be fed from it without sharing any computation.
+
+Shapes follow the "Llama 3.1 8B · Grouped-query attention" page (in/out contract:
+x [B,T,4096], R [T,64 pairs]; parameter table: W_Q 4096x4096, W_K and W_V 4096x(8x128),
+W_O 4096x4096) and the catalogue entry quoted there (dim 4096, n_heads 32,
+n_kv_heads 8, rope_theta 500000).  Weights use the [out, in] storage of the quoted
+fairscale linear layers ("we allocate the transpose").
+
+Draw order for one workload, from one ``torch.Generator('cpu').manual_seed(seed)``:
+x, W_Q, W_K, W_V, W_O, then (decode only) cache_K, cache_V.  Each draw is
+``randn(float32) * std`` rounded to bf16 with round-to-nearest-even.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+DIM = 4096
+N_HEADS = 32
+N_KV_HEADS = 8
+HEAD_DIM = DIM // N_HEADS  # 128
+N_PAIRS = HEAD_DIM // 2  # 64
+ROPE_THETA = 500000.0
+
+X_STD = 1.0
+W_STD = 0.02
+CACHE_STD = 1.0
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One synthetic workload: a prefill of B sequences of T tokens, or a decode step."""
+
+    name: str
+    kind: str  # "prefill" | "decode"
+    B: int
+    T: int
+    seed: int
+    causal: bool = True
+    start_pos: int = 0
+    S_max: int = 0  # 0 -> start_pos + T
+
+    @property
+    def s_max(self) -> int:
+        return self.S_max if self.S_max else self.start_pos + self.T
+
+    @property
+    def n_tok(self) -> int:
+        return self.B * self.T
+
+
+# The five workloads the block is measured and checked on.
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("prefill_b1_t16", "prefill", B=1, T=16, seed=0),
+        Workload("prefill_b1_t2048", "prefill", B=1, T=2048, seed=1),
+        Workload("prefill_b4_t8192", "prefill", B=4, T=8192, seed=2),
+        Workload("decode_b64_pos4095", "decode", B=64, T=1, seed=3, start_pos=4095, S_max=4096),
+        Workload("prefill_b1_t32768", "prefill", B=1, T=32768, seed=4),
+    ]
+}
+
+
+def _draw(gen: torch.Generator, shape, std: float) -> torch.Tensor:
+    return (torch.randn(*shape, generator=gen, dtype=torch.float32) * std).to(torch.bfloat16)
+
+
+@dataclass
+class BlockInputs:
+    x: torch.Tensor  # [B, T, 4096] bf16
+    wq: torch.Tensor  # [4096, 4096] bf16, [out, in]
+    wk: torch.Tensor  # [1024, 4096] bf16
+    wv: torch.Tensor  # [1024, 4096] bf16
+    wo: torch.Tensor  # [4096, 4096] bf16
+    R: torch.Tensor  # [T, 64, 2] fp32 (cos, sin) for positions start_pos .. start_pos+T-1
+    cache_k: torch.Tensor | None = None  # [B, S_max, 8, 128] bf16 (decode: pre-filled)
+    cache_v: torch.Tensor | None = None
+    meta: dict = field(default_factory=dict)
+
+
+def rope_table(positions, head_dim: int = HEAD_DIM, theta: float = ROPE_THETA) -> torch.Tensor:
+    """Rotation table R[t, j] = (cos(p_t w_j), sin(p_t w_j)), w_j = theta^(-2j/head_dim).
+
+    The pages name R as an input of the block ([T positions, 64 pairs]) but do not print
+    its generator; this is the standard unscaled form with the catalogue's theta.  Angles
+    are formed in fp64 and cos/sin rounded once to fp32.  Both the CUDA path and the
+    oracle read this same array, so the choice of generator does not affect parity.
+    """
+    p = np.asarray(positions, dtype=np.float64).reshape(-1, 1)
+    j = np.arange(head_dim // 2, dtype=np.float64).reshape(1, -1)
+    w = theta ** (-(2.0 * j) / head_dim)
+    ang = p * w
+    out = np.stack([np.cos(ang), np.sin(ang)], axis=-1).astype(np.float32)
+    return torch.from_numpy(np.ascontiguousarray(out))
+
+
+def make_weights(gen: torch.Generator, dim: int = DIM, n_heads: int = N_HEADS,
+                 n_kv_heads: int = N_KV_HEADS):
+    hd = dim // n_heads
+    wq = _draw(gen, (n_heads * hd, dim), W_STD)
+    wk = _draw(gen, (n_kv_heads * hd, dim), W_STD)
+    wv = _draw(gen, (n_kv_heads * hd, dim), W_STD)
+    wo = _draw(gen, (dim, n_heads * hd), W_STD)
+    return wq, wk, wv, wo
+
+
+def make_inputs(w: Workload | str, *, T: int | None = None, B: int | None = None) -> BlockInputs:
+    """Draw the inputs of a workload.  ``T``/``B`` override the sizes (same seed and draw
+    order) so that small parity cases keep the workload's value distributions."""
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    Bv = w.B if B is None else B
+    Tv = w.T if T is None else T
+    gen = torch.Generator("cpu").manual_seed(w.seed)
+    x = _draw(gen, (Bv, Tv, DIM), X_STD)
+    wq, wk, wv, wo = make_weights(gen)
+    cache_k = cache_v = None
+    s_max = w.S_max if w.S_max else w.start_pos + Tv
+    if w.kind == "decode":
+        cache_k = _draw(gen, (Bv, s_max, N_KV_HEADS, HEAD_DIM), CACHE_STD)
+        cache_v = _draw(gen, (Bv, s_max, N_KV_HEADS, HEAD_DIM), CACHE_STD)
+    R = rope_table(np.arange(w.start_pos, w.start_pos + Tv))
+    return BlockInputs(x, wq, wk, wv, wo, R, cache_k, cache_v,
+                       meta=dict(name=w.name, kind=w.kind, B=Bv, T=Tv, seed=w.seed,
+                                 causal=w.causal, start_pos=w.start_pos, S_max=s_max))
+
+
+def make_custom(seed: int, B: int, T: int, *, start_pos: int = 0, S_max: int | None = None,
+                fill_cache: bool = False) -> BlockInputs:
+    """Inputs for an arbitrary (B, T, start_pos) case with the same distributions."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    x = _draw(gen, (B, T, DIM), X_STD)
+    wq, wk, wv, wo = make_weights(gen)
+    s_max = S_max if S_max else start_pos + T
+    cache_k = cache_v = None
+    if fill_cache:
+        cache_k = _draw(gen, (B, s_max, N_KV_HEADS, HEAD_DIM), CACHE_STD)
+        cache_v = _draw(gen, (B, s_max, N_KV_HEADS, HEAD_DIM), CACHE_STD)
+    R = rope_table(np.arange(start_pos, start_pos + T))
+    return BlockInputs(x, wq, wk, wv, wo, R, cache_k, cache_v,
+                       meta=dict(name=f"custom_s{seed}_b{B}_t{T}_p{start_pos}", kind="prefill",
+                                 B=B, T=T, seed=seed, causal=True, start_pos=start_pos,
+                                 S_max=s_max))
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    """Exact widening of a bf16/fp32 CPU tensor to a float64 numpy array."""
+    return t.detach().to("cpu").to(torch.float64).numpy()
