@@ -1,0 +1,153 @@
+/*
+ * gqa_attn.h — C ABI of the GB300 (sm_103a) grouped-query attention block forward.
+ *
+ * The block is the Llama-3 / Llama-3.1 8B attention sub-block described on the page
+ * "Llama 3.1 8B · Grouped-query attention" (step list "All 13 steps"; in/out contract
+ * x [B,T,4096], R [T,64 pairs], M [T queries, T keys] -> Delta_attn [B,T,4096];
+ * parameter table: W_Q 4096x4096, W_K and W_V 4096x(8x128), W_O 4096x4096).  It computes
+ *
+ *     Q = x W_Q,  K = x W_K,  V = x W_V                      (steps 1-3)
+ *     Q_r, K_r = pair rotation of Q, K by R                  (steps 4-5)
+ *     K_G[h] = K_r[h/4],  V_G[h] = V[h/4]                    (steps 6-7)
+ *     S = Q_r K_G^T,  S_s = S / sqrt(128),  S_m = S_s + M    (steps 8-10)
+ *     A = softmax over keys of S_m,  H = A V_G               (steps 11-12)
+ *     H merged to [B,T,4096],  Delta_attn = H W_O            (steps 13-14)
+ *
+ * Dimensions are fixed by the model catalogue quoted on that page: dim 4096, 32 query
+ * heads, 8 key/value heads, head width 128 (64 rotation pairs).  B, T, the cache length
+ * S_max and start_pos are runtime values.
+ *
+ * Conventions shared by every call below
+ *  - Every pointer argument named x, R, R_row, cache_k, cache_v, delta, wq, wk, wv, wo is
+ *    a DEVICE pointer (cudaMalloc / torch CUDA storage on the current device).  The
+ *    caller owns these buffers; the library borrows them for the duration of the
+ *    asynchronous work it enqueues and never frees them.
+ *  - bf16 tensors are IEEE bfloat16 bit patterns (uint16), row-major, densely packed.
+ *  - Every device pointer must be 16-byte aligned (GQA_ERR_ALIGN otherwise).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is enqueued on
+ *    it and the call returns without synchronising, except where noted.
+ *  - Arguments are validated on the host before anything is enqueued; on any error the
+ *    call enqueues nothing and returns a non-zero gqa_status.
+ *  - A context may be used from one stream at a time; calls on one context must not
+ *    overlap on different streams (they share the context's workspace).
+ *  - Kernels bound every wait on the device.  A wait that runs out records
+ *    GQA_ERR_TIMEOUT in the context's device status word and the kernel returns; read
+ *    it with attn_sync_status.
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+typedef struct CUstream_st *gqa_stream_t;
+
+typedef struct gqa_ctx gqa_ctx; /* opaque */
+
+typedef enum {
+    GQA_OK = 0,
+    GQA_ERR_INVALID_ARG = 1, /* null pointer / null context / bad flag */
+    GQA_ERR_SHAPE = 2,       /* B, T, S_max, start_pos out of range */
+    GQA_ERR_ALIGN = 3,       /* a device pointer is not 16-byte aligned */
+    GQA_ERR_CUDA = 4,        /* a CUDA runtime call failed (see attn_last_cuda_error) */
+    GQA_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out (device status word) */
+    GQA_ERR_OOM = 6,         /* workspace allocation failed */
+    GQA_ERR_DEVICE = 7       /* current device is not an sm_103 GPU */
+} gqa_status;
+
+#define GQA_DIM 4096
+#define GQA_N_HEADS 32
+#define GQA_N_KV_HEADS 8
+#define GQA_HEAD_DIM 128
+#define GQA_QKV_DIM 6144 /* 4096 query + 1024 key + 1024 value features */
+
+/*
+ * attn_create — build a context for one block on the current CUDA device.
+ *
+ * wq [4096,4096], wk [1024,4096], wv [1024,4096], wo [4096,4096]: bf16 device tensors in
+ * the [out, in] storage of the quoted fairscale ColumnParallelLinear / RowParallelLinear
+ * layers ("F.linear performs XA^T ... we allocate the transpose").  They are COPIED into
+ * memory the context owns (W_Q, W_K, W_V packed into one [6144,4096] matrix; W_O kept
+ * [4096,4096]); the caller may free its copies once the stream has passed this call.
+ * The copies are enqueued on `stream`.
+ * On success *out receives the context (to be released with attn_destroy).
+ * Errors: GQA_ERR_INVALID_ARG (null), GQA_ERR_ALIGN, GQA_ERR_DEVICE (not sm_103),
+ * GQA_ERR_OOM, GQA_ERR_CUDA.
+ */
+gqa_status attn_create(const void *wq, const void *wk, const void *wv, const void *wo,
+                       gqa_stream_t stream, gqa_ctx **out);
+
+/*
+ * attn_prefill — Delta_attn for T new positions of B sequences (steps 1-14).
+ *
+ * x       [B,T,4096] bf16: the block input, already normalised by the caller
+ *         (the page's x_attn = attention_norm(x)).
+ * R       [T,64,2] fp32: (cos, sin) of the rotation for positions start_pos+t,
+ *         t = 0..T-1, pair j (the page's R [T positions, 64 pairs]).
+ * causal  non-zero: M[t,s] = -inf for keys s > start_pos+t, else 0 (the quoted
+ *         triu(diagonal=1) mask hstacked after start_pos zero columns); zero: M = 0.
+ * cache_k, cache_v  [B,S_max,8,128] bf16 key / value cache.  Positions
+ *         0..start_pos-1 must already hold rotated keys (cache_k) and values (cache_v)
+ *         of the earlier positions; this call writes K_r and V of its T positions at
+ *         start_pos..start_pos+T-1, then attends over keys 0..start_pos+T-1.  Other
+ *         positions are neither read nor written.
+ * delta   [B,T,4096] fp32 output, fully overwritten.
+ * Requires B >= 1, T >= 1, start_pos >= 0, start_pos + T <= S_max, and
+ * B*T <= 262144, S_max <= 1048576.
+ * Intermediates (Q_r and H, bf16) live in the context's workspace, which grows on
+ * demand: a call that needs a larger workspace synchronises `stream` and reallocates
+ * (so the first call at a new maximum size is not capturable in a CUDA graph).
+ */
+gqa_status attn_prefill(gqa_ctx *ctx, const void *x, int B, int T, const float *R, int causal,
+                        void *cache_k, void *cache_v, int S_max, int start_pos, float *delta,
+                        gqa_stream_t stream);
+
+/*
+ * attn_decode — one new position per sequence (T = 1, no mask: every cached key is
+ * visible, as in the quoted forward when seqlen == 1).
+ *
+ * x       [B,1,4096] bf16 block input of the new token of each sequence.
+ * R_row   [1,64,2] fp32: rotation for position start_pos (shared by all sequences).
+ * cache_k, cache_v  [B,S_max,8,128] bf16; positions 0..start_pos-1 hold the earlier
+ *         rotated keys / values.  The new K_r, V are written at position start_pos,
+ *         then the token attends over keys 0..start_pos.
+ * delta   [B,1,4096] fp32 output.
+ * Requires 1 <= B <= 1024, 0 <= start_pos < S_max <= 1048576.
+ */
+gqa_status attn_decode(gqa_ctx *ctx, const void *x, int B, int start_pos, const float *R_row,
+                       void *cache_k, void *cache_v, int S_max, float *delta,
+                       gqa_stream_t stream);
+
+/*
+ * attn_sync_status — synchronise `stream`, then read and clear the context's device
+ * status word.  Returns GQA_OK, GQA_ERR_TIMEOUT (a bounded device wait ran out in some
+ * earlier call) or GQA_ERR_CUDA (the synchronisation itself failed).
+ */
+gqa_status attn_sync_status(gqa_ctx *ctx, gqa_stream_t stream);
+
+/*
+ * attn_debug_buffers — device pointers to the context's intermediates after the last
+ * call on it: q_r [B*T,4096] bf16 (rotated queries) and h [B*T,4096] bf16 (merged head
+ * outputs, the page's H after step 13).  Valid until the next call on the context.
+ * Either out-pointer may be NULL.  Returns GQA_ERR_INVALID_ARG for a null context.
+ */
+gqa_status attn_debug_buffers(gqa_ctx *ctx, const void **q_r, const void **h);
+
+/* attn_destroy — free everything the context owns (after synchronising the device).
+ * NULL is ignored. */
+void attn_destroy(gqa_ctx *ctx);
+
+/* attn_strerror — static description of a status code (never NULL). */
+const char *attn_strerror(gqa_status status);
+
+/* attn_last_cuda_error — the cudaError_t value of the last failing CUDA call made by
+ * this library on the calling thread (0 if none). */
+int attn_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H */

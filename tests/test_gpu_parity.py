@@ -1,0 +1,175 @@
+"""GPU parity of the C-ABI path against the fp64 oracle (element by element, seeded inputs).
+
+Sizes span several 128-row tiles with ragged tails; the full-size workloads are checked on
+sampled query rows / sequences that the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import gqa_oracle as orc
+from tests import gpu_util as gu
+from transformer_gqa_attention_gb300 import inputs as gin
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from transformer_gqa_attention_gb300 import _build
+    _build.build()
+
+
+def _run_prefill_case(inp, causal=True, check_intermediates=True):
+    blk = gu.Block(inp)
+    try:
+        B, T = inp.x.shape[:2]
+        x = inp.x.to(gu.DEV)
+        R = inp.R.to(gu.DEV)
+        ck, cv = gu.empty_cache(B, T)
+        delta = blk.prefill(x, R, ck, cv, causal=causal)
+        ref, ex = gu.oracle_prefill(blk, inp, causal=causal, keep=check_intermediates)
+        out = {}
+        if check_intermediates:
+            q_r, h = blk.intermediates(B * T)
+            out["K_r"] = gu.assert_close(gu.np64(ck), ex["K_r"], gu.TOL_BF16_REL_L1, gu.TOL_BF16_MAX, "K_r")
+            out["V"] = gu.assert_close(gu.np64(cv), ex["V"], gu.TOL_BF16_REL_L1, gu.TOL_BF16_MAX, "V")
+            out["Q_r"] = gu.assert_close(gu.np64(q_r).reshape(B, T, 32, 128), ex["Q_r"],
+                                         gu.TOL_BF16_REL_L1, gu.TOL_BF16_MAX, "Q_r")
+            out["H"] = gu.assert_close(gu.np64(h).reshape(B, T, 4096), ex["H"], gu.TOL_REL_L1,
+                                       gu.TOL_MAX, "H")
+        out["delta"] = gu.assert_close(gu.np64(delta), ref, what="delta")
+        return out
+    finally:
+        blk.close()
+
+
+def test_prefill_b1_t16_workload():
+    _run_prefill_case(gin.make_inputs("prefill_b1_t16"))
+
+
+@pytest.mark.parametrize("B,T", [(1, 1), (2, 3), (1, 64), (3, 17), (1, 129), (2, 200), (1, 1000)])
+def test_prefill_ragged_shapes(B, T):
+    _run_prefill_case(gin.make_custom(seed=100 + T, B=B, T=T))
+
+
+def test_prefill_non_causal():
+    _run_prefill_case(gin.make_custom(seed=7, B=2, T=300), causal=False)
+
+
+def test_prefill_b1_t2048_workload_full():
+    _run_prefill_case(gin.make_inputs("prefill_b1_t2048"), check_intermediates=False)
+
+
+@pytest.mark.parametrize("name", ["prefill_b4_t8192", "prefill_b1_t32768"])
+def test_prefill_large_workloads_sampled_rows(name):
+    inp = gin.make_inputs(name)
+    blk = gu.Block(inp)
+    try:
+        B, T = inp.x.shape[:2]
+        ck, cv = gu.empty_cache(B, T)
+        delta = blk.prefill(inp.x.to(gu.DEV), inp.R.to(gu.DEV), ck, cv)
+        rows = gu.sample_rows(T)
+        ref, _ = gu.oracle_prefill(blk, inp, rows=rows)
+        gu.assert_close(gu.np64(delta[:, rows]), ref, what=f"{name} delta rows")
+        # keys / values of a few positions land in the cache
+        wq, wk, wv, wo = blk.w64
+        pos = rows[:8]
+        x64 = gin.to_f64(inp.x[:, pos])
+        K = orc.rope(orc.linear(x64, wk).reshape(B, len(pos), 8, 128), gin.to_f64(inp.R[pos]))
+        gu.assert_close(gu.np64(ck[:, pos]), K, gu.TOL_BF16_REL_L1, gu.TOL_BF16_MAX, "cache K rows")
+    finally:
+        blk.close()
+
+
+def test_chunked_prefill_continues_from_cache():
+    B, T1, T2 = 2, 100, 77
+    inp = gin.make_custom(seed=21, B=B, T=T1 + T2)
+    blk = gu.Block(inp)
+    try:
+        x = inp.x.to(gu.DEV)
+        R = inp.R.to(gu.DEV)
+        ck, cv = gu.empty_cache(B, T1 + T2 + 5)
+        blk.prefill(x[:, :T1].contiguous(), R[:T1].contiguous(), ck, cv)
+        d2 = blk.prefill(x[:, T1:].contiguous(), R[T1:].contiguous(), ck, cv, start_pos=T1)
+        ref, _ = gu.oracle_prefill(blk, inp)
+        gu.assert_close(gu.np64(d2), ref[:, T1:], what="second chunk")
+    finally:
+        blk.close()
+
+
+def test_decode_small():
+    B, S_max, pos = 3, 300, 257
+    inp = gin.make_custom(seed=31, B=B, T=1, start_pos=pos, S_max=S_max, fill_cache=True)
+    blk = gu.Block(inp)
+    try:
+        ck = inp.cache_k.to(gu.DEV)
+        cv = inp.cache_v.to(gu.DEV)
+        delta = blk.decode(inp.x.to(gu.DEV), inp.R.to(gu.DEV), ck, cv, pos)
+        wq, wk, wv, wo = blk.w64
+        ref, ex = orc.attention_decode(gin.to_f64(inp.x), wq, wk, wv, wo, gin.to_f64(inp.R),
+                                       gin.to_f64(inp.cache_k), gin.to_f64(inp.cache_v), pos)
+        gu.assert_close(gu.np64(delta), ref, what="decode delta")
+        gu.assert_close(gu.np64(ck[:, pos]), ex["cache_k"][:, pos], gu.TOL_BF16_REL_L1, gu.TOL_BF16_MAX,
+                        "new cache K")
+        # untouched cache entries stay bit-identical
+        assert torch.equal(ck[:, :pos].cpu(), inp.cache_k[:, :pos])
+        assert torch.equal(cv[:, pos + 1:].cpu(), inp.cache_v[:, pos + 1:])
+    finally:
+        blk.close()
+
+
+def test_decode_b64_pos4095_workload_sampled_sequences():
+    inp = gin.make_inputs("decode_b64_pos4095")
+    pos = 4095
+    blk = gu.Block(inp)
+    try:
+        ck = inp.cache_k.to(gu.DEV)
+        cv = inp.cache_v.to(gu.DEV)
+        delta = blk.decode(inp.x.to(gu.DEV), inp.R.to(gu.DEV), ck, cv, pos)
+        wq, wk, wv, wo = blk.w64
+        for b in (0, 17, 63):
+            ref, _ = orc.attention_decode(gin.to_f64(inp.x[b:b + 1]), wq, wk, wv, wo, gin.to_f64(inp.R),
+                                          gin.to_f64(inp.cache_k[b:b + 1]), gin.to_f64(inp.cache_v[b:b + 1]),
+                                          pos)
+            gu.assert_close(gu.np64(delta[b:b + 1]), ref, what=f"decode seq {b}")
+    finally:
+        blk.close()
+
+
+def test_decode_equals_last_prefill_row_on_gpu():
+    B, T = 2, 150
+    inp = gin.make_custom(seed=41, B=B, T=T)
+    blk = gu.Block(inp)
+    try:
+        x = inp.x.to(gu.DEV)
+        R = inp.R.to(gu.DEV)
+        ck, cv = gu.empty_cache(B, T)
+        dp = blk.prefill(x, R, ck, cv)
+        dd = blk.decode(x[:, T - 1:].contiguous(), R[T - 1:].contiguous(), ck, cv, T - 1)
+        l1, mx = gu.metrics(gu.np64(dd[:, 0]), gu.np64(dp[:, T - 1]))
+        assert l1 < 5e-3 and mx < 2e-2, (l1, mx)
+    finally:
+        blk.close()
+
+
+def test_causality_and_determinism_bit_exact():
+    B, T, t0 = 1, 300, 130
+    inp = gin.make_custom(seed=51, B=B, T=T)
+    blk = gu.Block(inp)
+    try:
+        x = inp.x.to(gu.DEV)
+        R = inp.R.to(gu.DEV)
+        ck, cv = gu.empty_cache(B, T)
+        d0 = blk.prefill(x, R, ck, cv).clone()
+        d1 = blk.prefill(x, R, ck, cv).clone()
+        assert torch.equal(d0, d1)
+        xp = x.clone()
+        xp[:, t0 + 1:] = -xp[:, t0 + 1:] * 3
+        d2 = blk.prefill(xp, R, ck, cv)
+        assert torch.equal(d2[:, :t0 + 1], d0[:, :t0 + 1])
+        assert not torch.equal(d2[:, t0 + 1:], d0[:, t0 + 1:])
+    finally:
+        blk.close()

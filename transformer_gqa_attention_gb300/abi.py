@@ -1,0 +1,129 @@
+"""ctypes binding of the C ABI in include/gqa_attn.h (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and forwards raw device
+pointers; all arithmetic of the block runs in the library's CUDA kernels.  Torch tensors
+are accepted for convenience and passed as ``tensor.data_ptr()``.  There is no fallback:
+if the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB_PATH
+
+GQA_OK = 0
+STATUS_NAMES = {0: "GQA_OK", 1: "GQA_ERR_INVALID_ARG", 2: "GQA_ERR_SHAPE", 3: "GQA_ERR_ALIGN",
+                4: "GQA_ERR_CUDA", 5: "GQA_ERR_TIMEOUT", 6: "GQA_ERR_OOM", 7: "GQA_ERR_DEVICE"}
+
+# Every symbol include/gqa_attn.h declares.
+EXPORTED = ("attn_create", "attn_prefill", "attn_decode", "attn_sync_status", "attn_debug_buffers",
+            "attn_destroy", "attn_strerror", "attn_last_cuda_error")
+
+_lib = None
+
+
+class GQAError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = lib().attn_strerror(status).decode()
+        extra = ""
+        if status == 4:
+            extra = f" (cudaError {lib().attn_last_cuda_error()})"
+        super().__init__(f"{fn} -> {STATUS_NAMES.get(status, status)}: {msg}{extra}")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libgqa_attn.so from the package directory (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it first (__graft_entry__.build() or "
+                           "python -m transformer_gqa_attention_gb300._build)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    L.attn_create.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(vp)]
+    L.attn_create.restype = i32
+    L.attn_prefill.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp, i32, i32, vp, vp]
+    L.attn_prefill.restype = i32
+    L.attn_decode.argtypes = [vp, vp, i32, i32, vp, vp, vp, i32, vp, vp]
+    L.attn_decode.restype = i32
+    L.attn_sync_status.argtypes = [vp, vp]
+    L.attn_sync_status.restype = i32
+    L.attn_debug_buffers.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp)]
+    L.attn_debug_buffers.restype = i32
+    L.attn_destroy.argtypes = [vp]
+    L.attn_destroy.restype = None
+    L.attn_strerror.argtypes = [i32]
+    L.attn_strerror.restype = ctypes.c_char_p
+    L.attn_last_cuda_error.argtypes = []
+    L.attn_last_cuda_error.restype = i32
+    _lib = L
+    return L
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, st: int):
+    if st != GQA_OK:
+        raise GQAError(fn, st)
+
+
+def attn_create(wq, wk, wv, wo, stream=None) -> int:
+    ctx = ctypes.c_void_p()
+    _check("attn_create", lib().attn_create(_ptr(wq), _ptr(wk), _ptr(wv), _ptr(wo), _stream(stream),
+                                            ctypes.byref(ctx)))
+    return ctx.value
+
+
+def attn_prefill(ctx, x, B, T, R, causal, cache_k, cache_v, S_max, start_pos, delta, stream=None):
+    _check("attn_prefill", lib().attn_prefill(ctx, _ptr(x), int(B), int(T), _ptr(R), int(bool(causal)),
+                                              _ptr(cache_k), _ptr(cache_v), int(S_max), int(start_pos),
+                                              _ptr(delta), _stream(stream)))
+
+
+def attn_decode(ctx, x, B, start_pos, R_row, cache_k, cache_v, S_max, delta, stream=None):
+    _check("attn_decode", lib().attn_decode(ctx, _ptr(x), int(B), int(start_pos), _ptr(R_row),
+                                            _ptr(cache_k), _ptr(cache_v), int(S_max), _ptr(delta),
+                                            _stream(stream)))
+
+
+def attn_sync_status(ctx, stream=None):
+    _check("attn_sync_status", lib().attn_sync_status(ctx, _stream(stream)))
+
+
+def attn_debug_buffers(ctx):
+    q, h = ctypes.c_void_p(), ctypes.c_void_p()
+    _check("attn_debug_buffers", lib().attn_debug_buffers(ctx, ctypes.byref(q), ctypes.byref(h)))
+    return q.value, h.value
+
+
+def attn_destroy(ctx):
+    if ctx:
+        lib().attn_destroy(ctx)
+
+
+def attn_strerror(status: int) -> str:
+    return lib().attn_strerror(int(status)).decode()
+
+
+def raw_status(fn_name: str, *args) -> int:
+    """Call an entry point with raw ctypes-compatible arguments and return its status code
+    (used by boundary tests that pass invalid arguments on purpose)."""
+    return getattr(lib(), fn_name)(*args)

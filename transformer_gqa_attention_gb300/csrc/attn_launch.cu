@@ -1,0 +1,40 @@
+// attn_launch.cu — instantiations of the prefill and decode attention kernels.
+#include "decode_attn.cuh"
+#include "flash_prefill.cuh"
+#include "launch.h"
+
+namespace gqa {
+
+cudaError_t configure_gemm_kernels();
+
+size_t flash_smem() { return FlashSmem::kBytes; }
+size_t decode_smem() { return DecodeSmem::kBytes; }
+
+cudaError_t configure_kernels() {
+  cudaError_t e = configure_gemm_kernels();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(flash_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           FlashSmem::kBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(decode_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              DecodeSmem::kBytes);
+}
+
+cudaError_t launch_flash_prefill(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                 const FlashParams& p, dim3 grid, cudaStream_t s) {
+  flash_prefill_kernel<<<grid, 192, FlashSmem::kBytes, s>>>(q, k, v, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_attn(const CUtensorMap& k, const CUtensorMap& v, const DecodeParams& p,
+                               dim3 grid, cudaStream_t s) {
+  decode_attn_kernel<<<grid, 160, DecodeSmem::kBytes, s>>>(k, v, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_combine(const DecodeParams& p, int B, cudaStream_t s) {
+  decode_combine_kernel<<<dim3(8, B), 128, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gqa

@@ -1,0 +1,259 @@
+// decode_attn.cuh — one new position per sequence (T = 1): steps 6-13 of
+// "Llama 3.1 8B · Grouped-query attention" against the KV cache, memory-bound.
+//
+// The 4 query heads of kv group g = h/4 share every key and value of that group
+// (K_G[h] = K_r[h/4], V_G[h] = V[h/4]), so one CTA serves (sequence b, group g, key
+// split) and streams each K/V byte of its split exactly once for all 4 heads.
+//
+//   warps 0..3  consumers: each takes 16 keys of every 64-key tile; S = q K^T and
+//               O += P V with mma.sync m16n8k16 (the 4 heads are rows 0..3 of the
+//               16-row A operand); online softmax in fp32 with quad-shuffle row max/sum
+//   warp 4      producer: 64-key K and V tiles by TMA (128-byte swizzle), 3 stages
+//
+// Each CTA writes an unnormalised partial (O, running max m, running sum l) per head;
+// decode_combine_kernel merges the splits (log-sum-exp) and writes H bf16 [B, 4096].
+#pragma once
+
+#include "params.h"
+#include "ptx.cuh"
+
+namespace gqa {
+
+struct DecodeSmem {
+  static constexpr int kHalf = kDecTileKeys * 64 * 2;  // 64 keys x 64 d bf16 = 8 KB
+  static constexpr int kTile = 2 * kHalf;              // 64 keys x 128 d
+  static constexpr int kStage = 2 * kTile;             // K + V
+  static constexpr int kRed = kDecStages * kStage;     // cross-warp reduction scratch
+  static constexpr int kRedBytes = 4 * 4 * 128 * 4 + 4 * 4 * 2 * 4;
+  static constexpr int kBar = kRed + kRedBytes;
+  static constexpr int kBytes = kBar + 128 + 1024;
+};
+
+// Byte offset of the 16-byte chunk `cd` (0..15, 8 d each) of key row `key` in a
+// 64-key x 128-d tile stored as two 128-byte-swizzled 64-d halves.
+__device__ __forceinline__ uint32_t dec_chunk_off(int key, int cd) {
+  return (cd >> 3) * DecodeSmem::kHalf + key * 128 + (((cd & 7) ^ (key & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(160)
+    decode_attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                       const DecodeParams p) {
+  using L = DecodeSmem;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* empty_bar = full_bar + kDecStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty_bar + kDecStages);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int split = blockIdx.x;
+  const int g = blockIdx.y;
+  const int b = blockIdx.z;
+  const int n_tiles_total = (p.kv_len + kDecTileKeys - 1) / kDecTileKeys;
+  const int t_begin = split * p.tiles_per_split;
+  const int t_end = min(n_tiles_total, t_begin + p.tiles_per_split);
+  const int my_tiles = t_end - t_begin;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 4);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 4) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      int issued = 0;
+      for (int i = 0; i < my_tiles; ++i) {
+        const int s = i % kDecStages;
+        const uint32_t ph = (i / kDecStages) & 1;
+        if (!mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&full_bar[s], L::kStage);
+        uint8_t* st = smem + s * L::kStage;
+        const int key0 = (t_begin + i) * kDecTileKeys;
+        tma_load_4d(st, &tmK, &full_bar[s], 0, g, key0, b);
+        tma_load_4d(st + L::kHalf, &tmK, &full_bar[s], 64, g, key0, b);
+        tma_load_4d(st + L::kTile, &tmV, &full_bar[s], 0, g, key0, b);
+        tma_load_4d(st + L::kTile + L::kHalf, &tmV, &full_bar[s], 64, g, key0, b);
+        ++issued;
+      }
+      if (*abort_flag) {
+        for (int i = (issued > kDecStages ? issued - kDecStages : 0); i < issued; ++i)
+          mbar_wait_drain(&full_bar[i % kDecStages], (i / kDecStages) & 1);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ consumers
+    // A operand (queries): rows 0..3 = heads 4g..4g+3 held by lanes 0..15, rows 4..15 zero.
+    const int qrow = lane >> 2;  // 0..7
+    const int qc = (lane & 3) * 2;
+    uint32_t qa[8][2];
+    {
+      const uint32_t* qp = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.q) + static_cast<size_t>(b) * 4096 +
+                                                             (g * 4 + (qrow & 3)) * 128);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        qa[kk][0] = (qrow < 4) ? __ldg(qp + (kk * 16 + qc) / 2) : 0u;
+        qa[kk][1] = (qrow < 4) ? __ldg(qp + (kk * 16 + qc + 8) / 2) : 0u;
+      }
+    }
+    float o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
+
+    const int kb = warp * 16;  // this warp's 16 keys inside each tile
+    bool ok = true;
+    for (int i = 0; i < my_tiles; ++i) {
+      const int s = i % kDecStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(&full_bar[s], (i / kDecStages) & 1, abort_flag, p.status));
+      if (!ok) break;
+      const uint32_t k_addr = smem_u32(smem + s * L::kStage);
+      const uint32_t v_addr = k_addr + L::kTile;
+
+      // S[16 x 16 keys]: two n8 tiles (keys kb..kb+7, kb+8..kb+15)
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const int mi = lane >> 3;  // matrix index supplied by this lane's address
+        const int key = kb + (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(k_addr + dec_chunk_off(key, 2 * kk + (mi & 1)), b0, b1, b2, b3);
+          mma_bf16_16816(sc[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+          mma_bf16_16816(sc[1], qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+        }
+      }
+      // mask keys beyond the cache length
+      const int kg0 = (t_begin + i) * kDecTileKeys + kb + qc;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          if (kg0 + nt * 8 + e >= p.kv_len) sc[nt][e] = -INFINITY;
+      float mx = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run, mx * p.scale_log2);
+      const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = fast_exp2(m_run - mu);
+      float pr[2][2];
+      float ls = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          pr[nt][e] = fast_exp2(fmaf(sc[nt][e], p.scale_log2, -mu));
+          ls += pr[nt][e];
+        }
+      ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+      ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+      l_run = l_run * alpha + ls;
+      m_run = m_new;
+#pragma unroll
+      for (int i2 = 0; i2 < 16; ++i2) {
+        o[i2][0] *= alpha;
+        o[i2][1] *= alpha;
+      }
+      // O[16 x 128] += P[16 x 16 keys] V[16 keys x 128]
+      const uint32_t pa0 = pack_bf16x2(pr[0][0], pr[0][1]);
+      const uint32_t pa2 = pack_bf16x2(pr[1][0], pr[1][1]);
+      {
+        const int mi = lane >> 3;
+        const int key = kb + (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+        for (int dp = 0; dp < 8; ++dp) {  // d blocks of 16
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(v_addr + dec_chunk_off(key, 2 * dp + (mi >> 1)), b0, b1, b2, b3);
+          mma_bf16_16816(o[2 * dp], pa0, 0u, pa2, 0u, b0, b1);
+          mma_bf16_16816(o[2 * dp + 1], pa0, 0u, pa2, 0u, b2, b3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);
+    }
+
+    // ---------------------------------------------------------- cross-warp merge
+    float* red_o = reinterpret_cast<float*>(smem + L::kRed);        // [4 warps][4 heads][128]
+    float* red_ml = red_o + 4 * 4 * 128;                             // [4 warps][4 heads][2]
+    if (lane < 16) {
+      const int hh = lane >> 2;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        red_o[(warp * 4 + hh) * 128 + nt * 8 + qc] = o[nt][0];
+        red_o[(warp * 4 + hh) * 128 + nt * 8 + qc + 1] = o[nt][1];
+      }
+      if ((lane & 3) == 0) {
+        red_ml[(warp * 4 + hh) * 2 + 0] = m_run;
+        red_ml[(warp * 4 + hh) * 2 + 1] = l_run;
+      }
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (ok && !*abort_flag) {
+      const int tid = threadIdx.x;  // 0..127 -> (head, 4 d values)
+      const int hh = tid >> 5;
+      const int d0 = (tid & 31) * 4;
+      float mw[4], M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        mw[w] = red_ml[(w * 4 + hh) * 2];
+        M = fmaxf(M, mw[w]);
+      }
+      const float Mu = (M == -INFINITY) ? 0.f : M;
+      float Ls = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float f = fast_exp2(mw[w] - Mu);
+        Ls += f * red_ml[(w * 4 + hh) * 2 + 1];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] += f * red_o[(w * 4 + hh) * 128 + d0 + e];
+      }
+      const size_t unit = (static_cast<size_t>(b) * 8 + g) * p.n_splits + split;
+      *reinterpret_cast<float4*>(p.part_o + (unit * 4 + hh) * 128 + d0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      if ((tid & 31) == 0) {
+        p.part_ml[(unit * 4 + hh) * 2 + 0] = M;
+        p.part_ml[(unit * 4 + hh) * 2 + 1] = Ls;
+      }
+    }
+  }
+}
+
+// Merge the key splits of each (b, g): H[b, h] = sum_s e^{m_s - M} O_s / sum_s e^{m_s - M} l_s.
+// grid (8, B), 128 threads: thread -> (head 0..3, 4 consecutive d).
+__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
+  const int g = blockIdx.x;
+  const int b = blockIdx.y;
+  const int hh = threadIdx.x >> 5;
+  const int d0 = (threadIdx.x & 31) * 4;
+  const size_t unit0 = (static_cast<size_t>(b) * 8 + g) * p.n_splits;
+  float M = -INFINITY;
+  for (int s = 0; s < p.n_splits; ++s) M = fmaxf(M, p.part_ml[((unit0 + s) * 4 + hh) * 2]);
+  const float Mu = (M == -INFINITY) ? 0.f : M;
+  float Ls = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < p.n_splits; ++s) {
+    const size_t u = (unit0 + s) * 4 + hh;
+    const float f = fast_exp2(p.part_ml[u * 2] - Mu);
+    Ls += f * p.part_ml[u * 2 + 1];
+    const float4 v = *reinterpret_cast<const float4*>(p.part_o + u * 128 + d0);
+    acc[0] += f * v.x;
+    acc[1] += f * v.y;
+    acc[2] += f * v.z;
+    acc[3] += f * v.w;
+  }
+  const float inv = 1.f / Ls;
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.H) + static_cast<size_t>(b) * 4096 + (g * 4 + hh) * 128 + d0;
+  uint2 w;
+  w.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  w.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+  *reinterpret_cast<uint2*>(dst) = w;
+}
+
+}  // namespace gqa

@@ -1,0 +1,486 @@
+// gqa_abi.cu — the C ABI declared in include/gqa_attn.h: argument validation, the
+// context (packed weights, status word, workspace), TMA descriptors and the launch
+// sequence of one block forward.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gqa_attn.h"
+#include "launch.h"
+#include "params.h"
+
+using namespace gqa;
+
+struct gqa_ctx {
+  int device = -1;
+  int num_sms = 0;
+  __nv_bfloat16* w_qkv = nullptr;  // [6144, 4096]: W_Q rows 0..4095, W_K 4096..5119, W_V 5120..6143
+  __nv_bfloat16* w_o = nullptr;    // [4096, 4096]
+  int* status = nullptr;           // device status word (kDevErr* bits)
+  uint8_t* ws = nullptr;           // workspace
+  size_t ws_bytes = 0;
+  const void* last_q = nullptr;
+  const void* last_h = nullptr;
+};
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+gqa_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return GQA_ERR_CUDA;
+}
+
+#define GQA_CUDA(call)                          \
+  do {                                          \
+    cudaError_t e_ = (call);                    \
+    if (e_ != cudaSuccess) return cuda_fail(e_); \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr long long kMaxTokens = 262144;
+constexpr long long kMaxSMax = 1048576;
+constexpr int kSkinnyMaxTokens = 64;     // at or below: swap-AB split-K projections
+constexpr int kDecodeMaxBatch = 1024;
+
+// ------------------------------------------------------------------ tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle; dims[0] innermost; strides in bytes for dims 1..
+bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+              const uint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) s[i] = strides[i];
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, s, b, e,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Row-major [rows, 4096] bf16 matrix, box 64 (K) x box_rows.
+bool map_rows_k4096(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  const uint64_t dims[2] = {4096, rows};
+  const uint64_t strides[1] = {4096 * 2};
+  const uint32_t box[2] = {64, box_rows};
+  return make_map(m, base, 2, dims, strides, box);
+}
+
+// KV cache [B, S_max, 8, 128] bf16 seen as (d, g, s < kv_len, b); box 64 d x key_rows.
+bool map_cache(CUtensorMap* m, const void* base, int B, int S_max, int kv_len, uint32_t key_rows) {
+  const uint64_t dims[4] = {128, 8, static_cast<uint64_t>(kv_len), static_cast<uint64_t>(B)};
+  const uint64_t strides[3] = {128 * 2, 1024 * 2, static_cast<uint64_t>(S_max) * 1024 * 2};
+  const uint32_t box[4] = {64, 1, key_rows, 1};
+  return make_map(m, base, 4, dims, strides, box);
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ workspace
+struct WsLayout {
+  size_t q_off, h_off, part_off, dec_o_off, dec_ml_off, total;
+};
+
+struct SkinnyPlan {
+  int n_tiles, tok_pad, splits_qkv, splits_o;
+};
+
+SkinnyPlan skinny_plan(int n_tok, int num_sms) {
+  SkinnyPlan s;
+  s.n_tiles = (n_tok + 63) / 64;
+  s.tok_pad = s.n_tiles * 64;
+  // about two CTAs per SM; each split keeps at least 4 k-blocks of 64
+  s.splits_qkv = std::max(1, std::min(16, (2 * num_sms) / (48 * s.n_tiles)));
+  s.splits_o = std::max(1, std::min(16, (2 * num_sms) / (32 * s.n_tiles)));
+  return s;
+}
+
+struct DecodePlan {
+  int n_splits, tiles_per_split;
+};
+
+DecodePlan decode_plan(int B, int kv_len, int num_sms) {
+  const int n_tiles = (kv_len + kDecTileKeys - 1) / kDecTileKeys;
+  // aim for ~8 waves of two CTAs per SM, at least 4 tiles (256 keys) per split
+  const long long units = static_cast<long long>(B) * 8;
+  const long long target = 16LL * num_sms;
+  int splits = static_cast<int>(std::max(1LL, (target + units - 1) / units));
+  splits = std::min(splits, std::max(1, n_tiles / 4));
+  DecodePlan d;
+  d.tiles_per_split = (n_tiles + splits - 1) / splits;
+  d.n_splits = (n_tiles + d.tiles_per_split - 1) / d.tiles_per_split;
+  return d;
+}
+
+WsLayout ws_layout(long long n_tok, const SkinnyPlan* sk, const DecodePlan* dp, int B_dec) {
+  WsLayout w{};
+  size_t off = 0;
+  w.q_off = off;
+  off = round_up(off + static_cast<size_t>(n_tok) * 4096 * 2, 256);
+  w.h_off = off;
+  off = round_up(off + static_cast<size_t>(n_tok) * 4096 * 2, 256);
+  w.part_off = off;
+  if (sk) {
+    const size_t a = static_cast<size_t>(sk->splits_qkv) * sk->tok_pad * 6144;
+    const size_t b = static_cast<size_t>(sk->splits_o) * sk->tok_pad * 4096;
+    off = round_up(off + std::max(a, b) * 4, 256);
+  }
+  w.dec_o_off = off;
+  w.dec_ml_off = off;
+  if (dp) {
+    const size_t units = static_cast<size_t>(B_dec) * 8 * dp->n_splits;
+    off = round_up(off + units * 4 * 128 * 4, 256);
+    w.dec_ml_off = off;
+    off = round_up(off + units * 4 * 2 * 4, 256);
+  }
+  w.total = off;
+  return w;
+}
+
+gqa_status ensure_ws(gqa_ctx* c, size_t bytes, cudaStream_t s) {
+  if (bytes <= c->ws_bytes) return GQA_OK;
+  GQA_CUDA(cudaStreamSynchronize(s));
+  if (c->ws) GQA_CUDA(cudaFree(c->ws));
+  c->ws = nullptr;
+  c->ws_bytes = 0;
+  const size_t want = round_up(bytes, 1 << 20);
+  if (cudaMalloc(&c->ws, want) != cudaSuccess) {
+    cudaGetLastError();
+    c->ws = nullptr;
+    return GQA_ERR_OOM;
+  }
+  c->ws_bytes = want;
+  return GQA_OK;
+}
+
+gqa_status check_device(gqa_ctx* c) {
+  int dev = -1;
+  GQA_CUDA(cudaGetDevice(&dev));
+  if (dev != c->device) return GQA_ERR_DEVICE;
+  return GQA_OK;
+}
+
+const float kScaleLog2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
+
+// Q/K/V projection + RoPE + cache write for n_tok tokens laid out [B, T] (steps 1-5).
+gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, void* ck, void* cv,
+                   int S_max, int start_pos, void* q_out, const WsLayout& w, const SkinnyPlan* sk,
+                   cudaStream_t s) {
+  GemmParams p{};
+  p.T = T;
+  p.S_max = S_max;
+  p.start_pos = start_pos;
+  p.status = c->status;
+  p.num_kb = 64;
+  CUtensorMap ta, tb;
+  if (sk) {
+    if (!map_rows_k4096(&ta, c->w_qkv, 6144, 128) || !map_rows_k4096(&tb, x, n_tok, 64))
+      return cuda_fail(cudaErrorInvalidValue);
+    p.M = 6144;
+    p.N = n_tok;
+    p.splits = sk->splits_qkv;
+    p.kb_per_split = 64 / p.splits;
+    p.n_tiles = sk->n_tiles;
+    p.out0 = c->ws + w.part_off;
+    p.ldo = 6144;
+    p.slab = static_cast<long long>(sk->tok_pad) * 6144;
+    const int grid = 48 * p.n_tiles * p.splits;
+    GQA_CUDA(launch_gemm_partial(ta, tb, p, grid, s));
+    QkvFinalizeParams f{};
+    f.part = reinterpret_cast<const float*>(c->ws + w.part_off);
+    f.slab = p.slab;
+    f.splits = p.splits;
+    f.n_tok = n_tok;
+    f.T = T;
+    f.S_max = S_max;
+    f.start_pos = start_pos;
+    f.R = R;
+    f.q = q_out;
+    f.cache_k = ck;
+    f.cache_v = cv;
+    GQA_CUDA(launch_qkv_finalize(f, s));
+  } else {
+    if (!map_rows_k4096(&ta, x, n_tok, 128) || !map_rows_k4096(&tb, c->w_qkv, 6144, 256))
+      return cuda_fail(cudaErrorInvalidValue);
+    p.M = n_tok;
+    p.N = 6144;
+    p.splits = 1;
+    p.kb_per_split = 64;
+    p.n_tiles = 24;
+    p.out0 = q_out;
+    p.out1 = ck;
+    p.out2 = cv;
+    p.R = R;
+    const int grid = ((n_tok + 127) / 128) * 24;
+    GQA_CUDA(launch_gemm_qkv_rope(ta, tb, p, grid, s));
+  }
+  return GQA_OK;
+}
+
+// Delta = H W_O^T (step 14).
+gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsLayout& w,
+                   const SkinnyPlan* sk, cudaStream_t s) {
+  GemmParams p{};
+  p.status = c->status;
+  p.num_kb = 64;
+  CUtensorMap ta, tb;
+  if (sk) {
+    if (!map_rows_k4096(&ta, c->w_o, 4096, 128) || !map_rows_k4096(&tb, h, n_tok, 64))
+      return cuda_fail(cudaErrorInvalidValue);
+    p.M = 4096;
+    p.N = n_tok;
+    p.splits = sk->splits_o;
+    p.kb_per_split = 64 / p.splits;
+    p.n_tiles = sk->n_tiles;
+    p.out0 = c->ws + w.part_off;
+    p.ldo = 4096;
+    p.slab = static_cast<long long>(sk->tok_pad) * 4096;
+    GQA_CUDA(launch_gemm_partial(ta, tb, p, 32 * p.n_tiles * p.splits, s));
+    OutFinalizeParams f{};
+    f.part = reinterpret_cast<const float*>(c->ws + w.part_off);
+    f.slab = p.slab;
+    f.splits = p.splits;
+    f.n_tok = n_tok;
+    f.delta = delta;
+    GQA_CUDA(launch_out_finalize(f, s));
+  } else {
+    if (!map_rows_k4096(&ta, h, n_tok, 128) || !map_rows_k4096(&tb, c->w_o, 4096, 256))
+      return cuda_fail(cudaErrorInvalidValue);
+    p.M = n_tok;
+    p.N = 4096;
+    p.splits = 1;
+    p.kb_per_split = 64;
+    p.n_tiles = 16;
+    p.out0 = delta;
+    p.ldo = 4096;
+    GQA_CUDA(launch_gemm_store_f32(ta, tb, p, ((n_tok + 127) / 128) * 16, s));
+  }
+  return GQA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_strerror(gqa_status st) {
+  switch (st) {
+    case GQA_OK: return "ok";
+    case GQA_ERR_INVALID_ARG: return "invalid argument (null pointer, null context or bad flag)";
+    case GQA_ERR_SHAPE: return "shape out of range (B, T, S_max or start_pos)";
+    case GQA_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case GQA_ERR_CUDA: return "CUDA runtime error (see attn_last_cuda_error)";
+    case GQA_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+    case GQA_ERR_OOM: return "workspace allocation failed";
+    case GQA_ERR_DEVICE: return "current device is not the context's sm_103 GPU";
+  }
+  return "unknown status";
+}
+
+int attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+gqa_status attn_create(const void* wq, const void* wk, const void* wv, const void* wo, gqa_stream_t stream,
+                       gqa_ctx** out) {
+  if (!out) return GQA_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!wq || !wk || !wv || !wo) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(wq) || !aligned16(wk) || !aligned16(wv) || !aligned16(wo)) return GQA_ERR_ALIGN;
+  int dev = -1;
+  GQA_CUDA(cudaGetDevice(&dev));
+  cudaDeviceProp prop;
+  GQA_CUDA(cudaGetDeviceProperties(&prop, dev));
+  if (prop.major != 10 || prop.minor != 3) return GQA_ERR_DEVICE;
+  if (!encode_fn()) return cuda_fail(cudaErrorNotSupported);
+  GQA_CUDA(configure_kernels());
+
+  gqa_ctx* c = new gqa_ctx();
+  c->device = dev;
+  c->num_sms = prop.multiProcessorCount;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  auto fail = [&](gqa_status st) {
+    attn_destroy(c);
+    return st;
+  };
+  if (cudaMalloc(&c->w_qkv, size_t(6144) * 4096 * 2) != cudaSuccess ||
+      cudaMalloc(&c->w_o, size_t(4096) * 4096 * 2) != cudaSuccess ||
+      cudaMalloc(&c->status, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(GQA_ERR_OOM);
+  }
+  const size_t wq_b = size_t(4096) * 4096 * 2, wkv_b = size_t(1024) * 4096 * 2;
+  cudaError_t e = cudaMemsetAsync(c->status, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(c->w_qkv, wq, wq_b, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(c->w_qkv) + wq_b, wk, wkv_b, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(c->w_qkv) + wq_b + wkv_b, wv, wkv_b,
+                        cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(c->w_o, wo, wq_b, cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) return fail(cuda_fail(e));
+  *out = c;
+  return GQA_OK;
+}
+
+gqa_status attn_prefill(gqa_ctx* c, const void* x, int B, int T, const float* R, int causal, void* cache_k,
+                        void* cache_v, int S_max, int start_pos, float* delta, gqa_stream_t stream) {
+  if (!c || !x || !R || !cache_k || !cache_v || !delta) return GQA_ERR_INVALID_ARG;
+  if (B < 1 || T < 1 || start_pos < 0 || S_max < 1 || S_max > kMaxSMax) return GQA_ERR_SHAPE;
+  if (static_cast<long long>(start_pos) + T > S_max) return GQA_ERR_SHAPE;
+  if (static_cast<long long>(B) * T > kMaxTokens) return GQA_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(R) || !aligned16(cache_k) || !aligned16(cache_v) || !aligned16(delta))
+    return GQA_ERR_ALIGN;
+  gqa_status st = check_device(c);
+  if (st != GQA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  const int n_tok = B * T;
+  SkinnyPlan sk_v = skinny_plan(n_tok, c->num_sms);
+  const SkinnyPlan* sk = n_tok <= kSkinnyMaxTokens ? &sk_v : nullptr;
+  const WsLayout w = ws_layout(n_tok, sk, nullptr, 0);
+  st = ensure_ws(c, w.total, s);
+  if (st != GQA_OK) return st;
+  void* q_r = c->ws + w.q_off;
+  void* h = c->ws + w.h_off;
+  c->last_q = q_r;
+  c->last_h = h;
+
+  st = run_qkv(c, x, n_tok, T, R, cache_k, cache_v, S_max, start_pos, q_r, w, sk, s);
+  if (st != GQA_OK) return st;
+
+  // steps 6-13: causal GQA flash attention over keys 0 .. start_pos+T-1
+  const int kv_len = start_pos + T;
+  CUtensorMap tq, tk, tv;
+  {
+    const uint64_t dims[3] = {4096, static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
+    const uint64_t strides[2] = {4096 * 2, static_cast<uint64_t>(T) * 4096 * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    if (!make_map(&tq, q_r, 3, dims, strides, box) || !map_cache(&tk, cache_k, B, S_max, kv_len, 128) ||
+        !map_cache(&tv, cache_v, B, S_max, kv_len, 128))
+      return cuda_fail(cudaErrorInvalidValue);
+  }
+  FlashParams fp{};
+  fp.B = B;
+  fp.T = T;
+  fp.S_max = S_max;
+  fp.start_pos = start_pos;
+  fp.causal = causal ? 1 : 0;
+  fp.n_qtiles = (T + 127) / 128;
+  fp.H = h;
+  fp.status = c->status;
+  fp.scale_log2 = kScaleLog2;
+  GQA_CUDA(launch_flash_prefill(tq, tk, tv, fp, dim3(B * 32, fp.n_qtiles), s));
+
+  return run_out(c, h, n_tok, delta, w, sk, s);
+}
+
+gqa_status attn_decode(gqa_ctx* c, const void* x, int B, int start_pos, const float* R_row, void* cache_k,
+                       void* cache_v, int S_max, float* delta, gqa_stream_t stream) {
+  if (!c || !x || !R_row || !cache_k || !cache_v || !delta) return GQA_ERR_INVALID_ARG;
+  if (B < 1 || B > kDecodeMaxBatch || start_pos < 0 || S_max < 1 || S_max > kMaxSMax || start_pos >= S_max)
+    return GQA_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(R_row) || !aligned16(cache_k) || !aligned16(cache_v) || !aligned16(delta))
+    return GQA_ERR_ALIGN;
+  gqa_status st = check_device(c);
+  if (st != GQA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  const int kv_len = start_pos + 1;
+  SkinnyPlan sk_v = skinny_plan(B, c->num_sms);
+  const SkinnyPlan* sk = B <= kSkinnyMaxTokens ? &sk_v : nullptr;
+  const DecodePlan dp = decode_plan(B, kv_len, c->num_sms);
+  const WsLayout w = ws_layout(B, sk, &dp, B);
+  st = ensure_ws(c, w.total, s);
+  if (st != GQA_OK) return st;
+  void* q_r = c->ws + w.q_off;
+  void* h = c->ws + w.h_off;
+  c->last_q = q_r;
+  c->last_h = h;
+
+  // steps 1-5 for the new token of each sequence (T = 1, position start_pos)
+  st = run_qkv(c, x, B, 1, R_row, cache_k, cache_v, S_max, start_pos, q_r, w, sk, s);
+  if (st != GQA_OK) return st;
+
+  // steps 6-13 against the cache (no mask: every key 0..start_pos is visible)
+  CUtensorMap tk, tv;
+  if (!map_cache(&tk, cache_k, B, S_max, kv_len, kDecTileKeys) ||
+      !map_cache(&tv, cache_v, B, S_max, kv_len, kDecTileKeys))
+    return cuda_fail(cudaErrorInvalidValue);
+  DecodeParams p{};
+  p.B = B;
+  p.kv_len = kv_len;
+  p.n_splits = dp.n_splits;
+  p.tiles_per_split = dp.tiles_per_split;
+  p.q = q_r;
+  p.part_o = reinterpret_cast<float*>(c->ws + w.dec_o_off);
+  p.part_ml = reinterpret_cast<float*>(c->ws + w.dec_ml_off);
+  p.H = h;
+  p.status = c->status;
+  p.scale_log2 = kScaleLog2;
+  GQA_CUDA(launch_decode_attn(tk, tv, p, dim3(dp.n_splits, 8, B), s));
+  GQA_CUDA(launch_decode_combine(p, B, s));
+
+  // step 14
+  return run_out(c, h, B, delta, w, sk, s);
+}
+
+gqa_status attn_sync_status(gqa_ctx* c, gqa_stream_t stream) {
+  if (!c) return GQA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  GQA_CUDA(cudaStreamSynchronize(s));
+  int v = 0;
+  GQA_CUDA(cudaMemcpy(&v, c->status, sizeof(int), cudaMemcpyDeviceToHost));
+  if (v != 0) {
+    GQA_CUDA(cudaMemset(c->status, 0, sizeof(int)));
+    if (v & kDevErrTimeout) return GQA_ERR_TIMEOUT;
+  }
+  return GQA_OK;
+}
+
+gqa_status attn_debug_buffers(gqa_ctx* c, const void** q_r, const void** h) {
+  if (!c) return GQA_ERR_INVALID_ARG;
+  if (q_r) *q_r = c->last_q;
+  if (h) *h = c->last_h;
+  return GQA_OK;
+}
+
+void attn_destroy(gqa_ctx* c) {
+  if (!c) return;
+  cudaDeviceSynchronize();
+  if (c->w_qkv) cudaFree(c->w_qkv);
+  if (c->w_o) cudaFree(c->w_o);
+  if (c->status) cudaFree(c->status);
+  if (c->ws) cudaFree(c->ws);
+  delete c;
+}
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// params.h — launch parameter blocks and constants shared by the kernels and the host
+// code (no device code here).
+#pragma once
+
+#include <cstdint>
+
+namespace gqa {
+
+// Status bits OR-ed into the context's device status word.
+constexpr int kDevErrTimeout = 1;
+
+// Upper bound for any single device-side wait (wall-clock, via %globaltimer).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s while draining after an abort
+
+enum EpiMode : int { kQkvRope = 0, kStoreF32 = 1, kPartialT = 2 };
+
+struct GemmParams {
+  int M, N;          // rows of A, rows of B
+  int num_kb;        // K / 64
+  int kb_per_split;  // k-blocks per split (last split takes the remainder)
+  int splits;
+  int n_tiles;       // ceil(N / BN)
+  // epilogue operands
+  void* out0;        // kQkvRope: Q_r [M,4096] bf16 | kStoreF32: D fp32 | kPartialT: partial base
+  void* out1;        // kQkvRope: cache_k
+  void* out2;        // kQkvRope: cache_v
+  const float* R;    // kQkvRope: [T,64,2]
+  int T, S_max, start_pos;
+  int ldo;           // kStoreF32: row stride (floats) | kPartialT: features per token row
+  long long slab;    // kPartialT: elements per split slab
+  int* status;
+};
+
+struct FlashParams {
+  int B, T, S_max, start_pos, causal;
+  int n_qtiles;
+  void* H;  // [B*T, 4096] bf16
+  int* status;
+  float scale_log2;  // log2(e) / sqrt(128)
+};
+
+constexpr int kDecStages = 3;
+constexpr int kDecTileKeys = 64;
+
+struct DecodeParams {
+  int B, kv_len, n_splits, tiles_per_split;
+  const void* q;  // [B, 4096] bf16 rotated queries
+  float* part_o;           // [B, 8, n_splits, 4, 128]
+  float* part_ml;          // [B, 8, n_splits, 4, 2]
+  void* H;        // [B, 4096] bf16 (combine output)
+  int* status;
+  float scale_log2;
+};
+
+}  // namespace gqa
