@@ -135,6 +135,35 @@ gqa_status attn_sync_status(gqa_ctx *ctx, gqa_stream_t stream);
  */
 gqa_status attn_debug_buffers(gqa_ctx *ctx, const void **q_r, const void **h);
 
+/*
+ * Per-kernel device timing (tracing).  Kernel kinds:
+ */
+enum {
+    GQA_KERNEL_QKV_GEMM = 0,       /* fused Q/K/V projection + RoPE + cache write (many tokens) */
+    GQA_KERNEL_QKV_SPLITK = 1,     /* Q/K/V projection, few tokens: split-K partials */
+    GQA_KERNEL_QKV_FINALIZE = 2,   /* split-K sum + RoPE + cache write */
+    GQA_KERNEL_FLASH_PREFILL = 3,  /* causal GQA attention, prefill */
+    GQA_KERNEL_DECODE_ATTN = 4,    /* split-KV attention, decode */
+    GQA_KERNEL_DECODE_COMBINE = 5, /* merge of the key splits */
+    GQA_KERNEL_OUT_GEMM = 6,       /* Delta = H W_O^T (many tokens) */
+    GQA_KERNEL_OUT_SPLITK = 7,     /* Delta = H W_O^T, few tokens: split-K partials */
+    GQA_KERNEL_OUT_FINALIZE = 8,   /* split-K sum into Delta */
+    GQA_KERNEL_KINDS = 9
+};
+
+/*
+ * attn_profile_begin — from now on, every kernel this context launches is bracketed by
+ * two CUDA events recorded on the launch stream (up to 65536 launches).  Recording adds
+ * two event records per launch and nothing else.
+ * attn_profile_end — stop recording, synchronise `stream`, and write, per kernel kind,
+ * the summed device time in milliseconds (ms_per_kind[GQA_KERNEL_KINDS]) and the number
+ * of launches (launches_per_kind[GQA_KERNEL_KINDS]) since attn_profile_begin.  Either
+ * output may be NULL.  Errors: GQA_ERR_INVALID_ARG (null context), GQA_ERR_CUDA.
+ */
+gqa_status attn_profile_begin(gqa_ctx *ctx);
+gqa_status attn_profile_end(gqa_ctx *ctx, double *ms_per_kind, int *launches_per_kind,
+                            gqa_stream_t stream);
+
 /* attn_destroy — free everything the context owns (after synchronising the device).
  * NULL is ignored. */
 void attn_destroy(gqa_ctx *ctx);

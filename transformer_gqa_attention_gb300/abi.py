@@ -18,7 +18,12 @@ STATUS_NAMES = {0: "GQA_OK", 1: "GQA_ERR_INVALID_ARG", 2: "GQA_ERR_SHAPE", 3: "G
 
 # Every symbol include/gqa_attn.h declares.
 EXPORTED = ("attn_create", "attn_prefill", "attn_decode", "attn_sync_status", "attn_debug_buffers",
-            "attn_destroy", "attn_strerror", "attn_last_cuda_error")
+            "attn_profile_begin", "attn_profile_end", "attn_destroy", "attn_strerror",
+            "attn_last_cuda_error")
+
+# Kernel kinds of attn_profile_end (GQA_KERNEL_* in include/gqa_attn.h).
+KERNEL_KINDS = ("qkv_gemm", "qkv_splitk", "qkv_finalize", "flash_prefill", "decode_attn",
+                "decode_combine", "out_gemm", "out_splitk", "out_finalize")
 
 _lib = None
 
@@ -53,6 +58,10 @@ def lib() -> ctypes.CDLL:
     L.attn_sync_status.restype = i32
     L.attn_debug_buffers.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp)]
     L.attn_debug_buffers.restype = i32
+    L.attn_profile_begin.argtypes = [vp]
+    L.attn_profile_begin.restype = i32
+    L.attn_profile_end.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i32), vp]
+    L.attn_profile_end.restype = i32
     L.attn_destroy.argtypes = [vp]
     L.attn_destroy.restype = None
     L.attn_strerror.argtypes = [i32]
@@ -112,6 +121,19 @@ def attn_debug_buffers(ctx):
     q, h = ctypes.c_void_p(), ctypes.c_void_p()
     _check("attn_debug_buffers", lib().attn_debug_buffers(ctx, ctypes.byref(q), ctypes.byref(h)))
     return q.value, h.value
+
+
+def attn_profile_begin(ctx):
+    _check("attn_profile_begin", lib().attn_profile_begin(ctx))
+
+
+def attn_profile_end(ctx, stream=None):
+    """-> {kind: (total_ms, launches)} for the launches since attn_profile_begin."""
+    n = len(KERNEL_KINDS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int * n)()
+    _check("attn_profile_end", lib().attn_profile_end(ctx, ms, cnt, _stream(stream)))
+    return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_KINDS)}
 
 
 def attn_destroy(ctx):

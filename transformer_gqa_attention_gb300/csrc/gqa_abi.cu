@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "gqa_attn.h"
 #include "launch.h"
@@ -27,6 +28,11 @@ struct gqa_ctx {
   size_t ws_bytes = 0;
   const void* last_q = nullptr;
   const void* last_h = nullptr;
+  // per-kernel device timing
+  bool profiling = false;
+  std::vector<cudaEvent_t> ev;        // 2 per recorded launch
+  std::vector<int> ev_kind;           // kind of each recorded launch
+  size_t ev_used = 0;                 // launches recorded so far
 };
 
 namespace {
@@ -191,6 +197,35 @@ gqa_status check_device(gqa_ctx* c) {
   return GQA_OK;
 }
 
+constexpr size_t kMaxProfiledLaunches = 65536;
+
+// RAII bracket of one kernel launch with two events when profiling is on.
+struct ProfScope {
+  gqa_ctx* c;
+  cudaStream_t s;
+  bool on;
+  ProfScope(gqa_ctx* c_, int kind, cudaStream_t s_) : c(c_), s(s_), on(false) {
+    if (c->profiling && c->ev_used < kMaxProfiledLaunches) {
+      if (c->ev.size() < 2 * (c->ev_used + 1)) {
+        cudaEvent_t a, b;
+        if (cudaEventCreate(&a) != cudaSuccess) return;
+        if (cudaEventCreate(&b) != cudaSuccess) { cudaEventDestroy(a); return; }
+        c->ev.push_back(a);
+        c->ev.push_back(b);
+        c->ev_kind.push_back(kind);
+      }
+      c->ev_kind[c->ev_used] = kind;
+      on = cudaEventRecord(c->ev[2 * c->ev_used], s) == cudaSuccess;
+    }
+  }
+  ~ProfScope() {
+    if (on) {
+      cudaEventRecord(c->ev[2 * c->ev_used + 1], s);
+      ++c->ev_used;
+    }
+  }
+};
+
 const float kScaleLog2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
 
 // Q/K/V projection + RoPE + cache write for n_tok tokens laid out [B, T] (steps 1-5).
@@ -216,7 +251,7 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
     p.ldo = 6144;
     p.slab = static_cast<long long>(sk->tok_pad) * 6144;
     const int grid = 48 * p.n_tiles * p.splits;
-    GQA_CUDA(launch_gemm_partial(ta, tb, p, grid, s));
+    { ProfScope ps(c, GQA_KERNEL_QKV_SPLITK, s); GQA_CUDA(launch_gemm_partial(ta, tb, p, grid, s)); }
     QkvFinalizeParams f{};
     f.part = reinterpret_cast<const float*>(c->ws + w.part_off);
     f.slab = p.slab;
@@ -229,7 +264,7 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
     f.q = q_out;
     f.cache_k = ck;
     f.cache_v = cv;
-    GQA_CUDA(launch_qkv_finalize(f, s));
+    { ProfScope ps(c, GQA_KERNEL_QKV_FINALIZE, s); GQA_CUDA(launch_qkv_finalize(f, s)); }
   } else {
     if (!map_rows_k4096(&ta, x, n_tok, 128) || !map_rows_k4096(&tb, c->w_qkv, 6144, 256))
       return cuda_fail(cudaErrorInvalidValue);
@@ -243,7 +278,7 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
     p.out2 = cv;
     p.R = R;
     const int grid = ((n_tok + 127) / 128) * 24;
-    GQA_CUDA(launch_gemm_qkv_rope(ta, tb, p, grid, s));
+    { ProfScope ps(c, GQA_KERNEL_QKV_GEMM, s); GQA_CUDA(launch_gemm_qkv_rope(ta, tb, p, grid, s)); }
   }
   return GQA_OK;
 }
@@ -266,14 +301,14 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
     p.out0 = c->ws + w.part_off;
     p.ldo = 4096;
     p.slab = static_cast<long long>(sk->tok_pad) * 4096;
-    GQA_CUDA(launch_gemm_partial(ta, tb, p, 32 * p.n_tiles * p.splits, s));
+    { ProfScope ps(c, GQA_KERNEL_OUT_SPLITK, s); GQA_CUDA(launch_gemm_partial(ta, tb, p, 32 * p.n_tiles * p.splits, s)); }
     OutFinalizeParams f{};
     f.part = reinterpret_cast<const float*>(c->ws + w.part_off);
     f.slab = p.slab;
     f.splits = p.splits;
     f.n_tok = n_tok;
     f.delta = delta;
-    GQA_CUDA(launch_out_finalize(f, s));
+    { ProfScope ps(c, GQA_KERNEL_OUT_FINALIZE, s); GQA_CUDA(launch_out_finalize(f, s)); }
   } else {
     if (!map_rows_k4096(&ta, h, n_tok, 128) || !map_rows_k4096(&tb, c->w_o, 4096, 256))
       return cuda_fail(cudaErrorInvalidValue);
@@ -284,7 +319,7 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
     p.n_tiles = 16;
     p.out0 = delta;
     p.ldo = 4096;
-    GQA_CUDA(launch_gemm_store_f32(ta, tb, p, ((n_tok + 127) / 128) * 16, s));
+    { ProfScope ps(c, GQA_KERNEL_OUT_GEMM, s); GQA_CUDA(launch_gemm_store_f32(ta, tb, p, ((n_tok + 127) / 128) * 16, s)); }
   }
   return GQA_OK;
 }
@@ -398,7 +433,7 @@ gqa_status attn_prefill(gqa_ctx* c, const void* x, int B, int T, const float* R,
   fp.H = h;
   fp.status = c->status;
   fp.scale_log2 = kScaleLog2;
-  GQA_CUDA(launch_flash_prefill(tq, tk, tv, fp, dim3(B * 32, fp.n_qtiles), s));
+  { ProfScope ps(c, GQA_KERNEL_FLASH_PREFILL, s); GQA_CUDA(launch_flash_prefill(tq, tk, tv, fp, dim3(B * 32, fp.n_qtiles), s)); }
 
   return run_out(c, h, n_tok, delta, w, sk, s);
 }
@@ -446,8 +481,8 @@ gqa_status attn_decode(gqa_ctx* c, const void* x, int B, int start_pos, const fl
   p.H = h;
   p.status = c->status;
   p.scale_log2 = kScaleLog2;
-  GQA_CUDA(launch_decode_attn(tk, tv, p, dim3(dp.n_splits, 8, B), s));
-  GQA_CUDA(launch_decode_combine(p, B, s));
+  { ProfScope ps(c, GQA_KERNEL_DECODE_ATTN, s); GQA_CUDA(launch_decode_attn(tk, tv, p, dim3(dp.n_splits, 8, B), s)); }
+  { ProfScope ps(c, GQA_KERNEL_DECODE_COMBINE, s); GQA_CUDA(launch_decode_combine(p, B, s)); }
 
   // step 14
   return run_out(c, h, B, delta, w, sk, s);
@@ -473,9 +508,40 @@ gqa_status attn_debug_buffers(gqa_ctx* c, const void** q_r, const void** h) {
   return GQA_OK;
 }
 
+gqa_status attn_profile_begin(gqa_ctx* c) {
+  if (!c) return GQA_ERR_INVALID_ARG;
+  c->profiling = true;
+  c->ev_used = 0;
+  return GQA_OK;
+}
+
+gqa_status attn_profile_end(gqa_ctx* c, double* ms_per_kind, int* launches_per_kind, gqa_stream_t stream) {
+  if (!c) return GQA_ERR_INVALID_ARG;
+  c->profiling = false;
+  GQA_CUDA(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+  double ms[GQA_KERNEL_KINDS] = {0};
+  int n[GQA_KERNEL_KINDS] = {0};
+  for (size_t i = 0; i < c->ev_used; ++i) {
+    float t = 0.f;
+    GQA_CUDA(cudaEventElapsedTime(&t, c->ev[2 * i], c->ev[2 * i + 1]));
+    const int k = c->ev_kind[i];
+    if (k >= 0 && k < GQA_KERNEL_KINDS) {
+      ms[k] += t;
+      n[k] += 1;
+    }
+  }
+  c->ev_used = 0;
+  for (int k = 0; k < GQA_KERNEL_KINDS; ++k) {
+    if (ms_per_kind) ms_per_kind[k] = ms[k];
+    if (launches_per_kind) launches_per_kind[k] = n[k];
+  }
+  return GQA_OK;
+}
+
 void attn_destroy(gqa_ctx* c) {
   if (!c) return;
   cudaDeviceSynchronize();
+  for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
   if (c->w_qkv) cudaFree(c->w_qkv);
   if (c->w_o) cudaFree(c->w_o);
   if (c->status) cudaFree(c->status);
