@@ -1,0 +1,452 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 grouped-query attention block forward; prints ONE JSON line.
+
+Default workload: prefill of B=1 sequence of T=2048 tokens (dim 4096, 32 q / 8 kv heads,
+d_h 128, bf16 inputs, random N(0, 0.02) weights, theta=500000 RoPE table, causal mask,
+fp32 output).  A step is one full block forward (Q/K/V projection + RoPE + cache write,
+causal GQA attention, W_O projection) through the C ABI, inputs resident in HBM.  L2 is
+flushed (256 MiB write) before every timed step, outside the step's events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+N > 1 runs under torchrun: one rank per GPU, each rank runs its own replica of the
+workload (weak scaling; the path has no cross-sequence exchange), max time over ranks.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from transformer_gqa_attention_gb300 import inputs as gin  # noqa: E402
+
+METRIC = "GQA block tokens/s & TFLOP/s (prefill), HBM GB/s (decode), % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ------------------------------------------------------------------ accounting
+def prefill_flops(B, T, start_pos=0, causal=True):
+    """Algorithmic FLOPs: 2 x 41,943,040 per token for the projections plus 4*128 per
+    visible (query, key) pair per query head (QK^T and PV)."""
+    proj = 2 * 41_943_040 * B * T
+    if causal:
+        pairs = T * start_pos + T * (T + 1) // 2
+    else:
+        pairs = T * (start_pos + T)
+    return proj, 4 * 128 * 32 * pairs * B
+
+
+def decode_bytes(B, kv_len):
+    """Minimum HBM bytes of one decode step: the K/V cache read (kv_len keys x 8 heads x
+    128 x bf16, K and V), the weights (W_QKV + W_O), x in, Delta out (fp32), the new K/V
+    entries written."""
+    kv = B * kv_len * 8 * 128 * 2 * 2
+    w = 41_943_040 * 2
+    return kv + w + B * 4096 * 2 + B * 4096 * 4 + B * 1024 * 2 * 2
+
+
+def kernel_work(kind, w: gin.Workload):
+    """(bound, algorithmic work per launch, unit) of one kernel kind on the workload."""
+    n_tok = w.n_tok
+    if kind == "qkv_gemm":
+        return "tensor", 2.0 * n_tok * 4096 * 6144, "TFLOP/s"
+    if kind == "out_gemm":
+        return "tensor", 2.0 * n_tok * 4096 * 4096, "TFLOP/s"
+    if kind == "flash_prefill":
+        return "tensor", float(prefill_flops(w.B, w.T, w.start_pos, w.causal)[1]), "TFLOP/s"
+    if kind == "decode_attn":
+        kv_len = w.start_pos + 1
+        return "hbm", float(w.B * kv_len * 8 * 128 * 2 * 2 + w.B * 4096 * 2), "GB/s"
+    if kind == "qkv_splitk":
+        return "hbm", float(6144 * 4096 * 2 + n_tok * 4096 * 2), "GB/s"
+    if kind == "out_splitk":
+        return "hbm", float(4096 * 4096 * 2 + n_tok * 4096 * 2), "GB/s"
+    return None, None, None
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "transformer_gqa_attention_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kind, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel sources for this workload; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kind)
+    if not e or e.get("source_digest") != source_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        sel = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            if uuid:
+                sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                    "-lms", "200", *sel]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons, power = [], [], set(), []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if n_gpus > 1 and world != n_gpus:
+        raise SystemExit(f"--gpus {n_gpus} needs torchrun with {n_gpus} ranks (WORLD_SIZE={world})")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v, world, device):
+    if world == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle timing
+def oracle_sample_step(inp, w: gin.Workload, n_tokens: int, seqs: int, w64):
+    """Run the fp64 oracle on a bounded sample: for a prefill, the first n_tokens positions
+    of `seqs` sequences (a causal prefix is the exact computation of those rows); for a
+    decode, `seqs` sequences.  Returns (seconds, units processed, bytes for decode)."""
+    from oracle import gqa_oracle as orc
+    wq, wk, wv, wo = w64
+    t0 = time.perf_counter()
+    if w.kind == "prefill":
+        x = gin.to_f64(inp.x[:seqs, :n_tokens])
+        R = gin.to_f64(inp.R[:n_tokens])
+        orc.attention_block(x, wq, wk, wv, wo, R, causal=w.causal)
+        units = seqs * n_tokens
+    else:
+        pos = w.start_pos
+        x = gin.to_f64(inp.x[:seqs])
+        ck = gin.to_f64(inp.cache_k[:seqs, :pos + 1])
+        cv = gin.to_f64(inp.cache_v[:seqs, :pos + 1])
+        orc.attention_decode(x, wq, wk, wv, wo, gin.to_f64(inp.R), ck, cv, pos)
+        units = seqs
+    return time.perf_counter() - t0, units
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_baseline(inp, w: gin.Workload, budget_s=15.0):
+    """Time the oracle as it stands on the host cores on a bounded sample (~budget_s)."""
+    w64 = [gin.to_f64(t) for t in (inp.wq, inp.wk, inp.wv, inp.wo)]
+    if w.kind == "prefill":
+        n = min(w.T, 2048)
+        seqs = 1
+        desc = f"oracle prefill of positions 0..{n - 1} of sequence 0"
+    else:
+        n = 1
+        seqs = min(w.B, 4)
+        desc = f"oracle decode of {seqs} of the {w.B} sequences"
+    times, units = [], 0
+    t_start = time.perf_counter()
+    while True:
+        dt, u = oracle_sample_step(inp, w, n, seqs, w64)
+        times.append(dt)
+        units += u
+        if time.perf_counter() - t_start > budget_s or len(times) >= 10:
+            break
+    total = sum(times)
+    if w.kind == "prefill":
+        value, unit = units / total, "tokens/s"
+    else:
+        per_seq = decode_bytes(1, w.start_pos + 1) - 41_943_040 * 2
+        value, unit = (len(times) * (seqs * per_seq + 41_943_040 * 2)) / total / 1e9, "GB/s"
+    return {"value": value, "unit": unit, "cores": cores(), "kind": "oracle",
+            "sample": f"{desc}, {len(times)} run(s), {total:.1f} s"}
+
+
+def run_reference(args, w, inp):
+    """The oracle as the reference arm: W untimed + K timed steps, each a bounded sample."""
+    w64 = [gin.to_f64(t) for t in (inp.wq, inp.wk, inp.wv, inp.wo)]
+    total_budget = 120.0
+    if w.kind == "prefill":
+        dt, _ = oracle_sample_step(inp, w, 32, 1, w64)  # calibration
+        per_tok = dt / 32
+        n = int(max(16, min(w.T, total_budget / max(1, args.steps + args.warmup) / per_tok)))
+        seqs = 1
+        desc = f"oracle prefill of positions 0..{n - 1} of sequence 0 per step"
+    else:
+        n, seqs = 1, 1
+        desc = "oracle decode of sequence 0 per step"
+    for _ in range(args.warmup):
+        oracle_sample_step(inp, w, n, seqs, w64)
+    times, units = [], 0
+    for _ in range(args.steps):
+        dt, u = oracle_sample_step(inp, w, n, seqs, w64)
+        times.append(dt)
+        units += u
+    total = sum(times)
+    ms = 1e3 * total / len(times)
+    if w.kind == "prefill":
+        value, unit = units / total, "tokens/s"
+    else:
+        value = len(times) * (decode_bytes(1, w.start_pos + 1)) / total / 1e9
+        unit = "GB/s"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"kind": "oracle", "cores": cores(), "sample": desc, "value": value,
+                             "unit": unit},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def workload_config(w: gin.Workload):
+    c = {"workload": w.name, "kind": w.kind, "B": w.B, "T": w.T, "start_pos": w.start_pos,
+         "S_max": w.s_max, "causal": w.causal, "dim": 4096, "n_heads": 32, "n_kv_heads": 8,
+         "head_dim": 128, "seed": w.seed, "l2": "flushed before every timed step (256 MiB write)"}
+    return c
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, w: gin.Workload, inp, world, rank, local):
+    from transformer_gqa_attention_gb300 import _build, abi
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    _build.build()
+    B, T = w.B, w.T
+    S_max = w.s_max
+    wts = [t.to(dev) for t in (inp.wq, inp.wk, inp.wv, inp.wo)]
+    ctx = abi.attn_create(*wts)
+    stream = torch.cuda.current_stream(dev)
+    x = inp.x.to(dev)
+    R = inp.R.to(dev)
+    if w.kind == "prefill":
+        ck = torch.zeros(B, S_max, 8, 128, dtype=torch.bfloat16, device=dev)
+        cv = torch.zeros_like(ck)
+        delta = torch.empty(B, T, 4096, dtype=torch.float32, device=dev)
+
+        def step(xd=x, Rd=R, out=delta):
+            abi.attn_prefill(ctx, xd, B, T, Rd, w.causal, ck, cv, S_max, w.start_pos, out, stream)
+    else:
+        ck = inp.cache_k.to(dev)
+        cv = inp.cache_v.to(dev)
+        delta = torch.empty(B, 1, 4096, dtype=torch.float32, device=dev)
+
+        def step(xd=x, Rd=R, out=delta):
+            abi.attn_decode(ctx, xd, B, w.start_pos, Rd, ck, cv, S_max, out, stream)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    abi.attn_sync_status(ctx, stream)
+
+    # ---------------- device-timed region
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    abi.attn_profile_begin(ctx)
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    prof = abi.attn_profile_end(ctx, stream)
+    clocks = sampler.stop() if sampler else None
+    abi.attn_sync_status(ctx, stream)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_local = sum(step_ms) / len(step_ms)
+    ms = max_over_ranks(ms_local, world, dev)
+
+    # ---------------- end to end through host buffers (pinned)
+    x_h = inp.x.pin_memory()
+    R_h = inp.R.pin_memory()
+    out_h = torch.empty(delta.shape, dtype=torch.float32).pin_memory()
+    x_d = torch.empty_like(x)
+    R_d = torch.empty_like(R)
+    e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        e_starts[i].record(stream)
+        x_d.copy_(x_h, non_blocking=True)
+        R_d.copy_(R_h, non_blocking=True)
+        step(x_d, R_d, delta)
+        out_h.copy_(delta, non_blocking=True)
+        e_ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(e_starts, e_ends)) / args.steps,
+                            world, dev)
+    h2d = x_h.numel() * x_h.element_size() + R_h.numel() * R_h.element_size()
+    d2h = out_h.numel() * out_h.element_size()
+    abi.attn_sync_status(ctx, stream)
+    abi.attn_destroy(ctx)
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    n = world
+    if w.kind == "prefill":
+        proj, attn = prefill_flops(B, T, w.start_pos, w.causal)
+        value = n * B * T / (ms / 1e3)
+        unit = "tokens/s"
+        e2e_value = n * B * T / (e2e_ms / 1e3)
+        extra = {"tflops": n * (proj + attn) / (ms / 1e3) / 1e12,
+                 "tflops_frac_of_" + peak_src: (proj + attn) / (ms / 1e3) / 1e12 / peaks["bf16_tflops"]}
+    else:
+        by = decode_bytes(B, w.start_pos + 1)
+        value = n * by / (ms / 1e3) / 1e9
+        unit = "GB/s"
+        e2e_value = n * by / (e2e_ms / 1e3) / 1e9
+        extra = {"tokens_per_s": n * B / (ms / 1e3),
+                 "hbm_frac_of_" + peak_src: by / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+
+    kinds = {k: v for k, v in prof.items() if v[1] > 0}
+    dom = max(kinds, key=lambda k: kinds[k][0])
+    bound, work, wunit = kernel_work(dom, w)
+    avg_ms = kinds[dom][0] / kinds[dom][1]
+    if bound == "tensor":
+        achieved = work / (avg_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+    else:
+        achieved = work / (avg_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+    roofline = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": wunit,
+                "frac": achieved / peak, "peak_source": f"{peak_src} (burst)" if bound == "tensor" else peak_src,
+                "traffic": ncu_traffic(dom, w.name), "work_per_launch": work,
+                "avg_launch_ms": avg_ms}
+    per_kernel = {k: {"ms_per_launch": v[0] / v[1], "launches": v[1], "share": v[0] / sum(x[0] for x in kinds.values())}
+                  for k, v in kinds.items()}
+    line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": n, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) x, N(0,0.02) weights)",
+            "config": workload_config(w), **extra, "roofline": roofline, "kernels": per_kernel,
+            "gpu_launches": int(sum(v[1] for v in kinds.values())),
+            "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "clocks": clocks}
+    if n == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, w)
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="prefill_b1_t2048", choices=sorted(gin.WORKLOADS))
+    ap.add_argument("--impl", default="gqa", choices=["gqa", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup(args.gpus)
+    w = gin.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w, gin.make_inputs(w))
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    inp = gin.make_inputs(w)
+    try:
+        run_gpu(args, w, inp, world, rank, local)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
