@@ -164,6 +164,38 @@ gqa_status attn_profile_begin(gqa_ctx *ctx);
 gqa_status attn_profile_end(gqa_ctx *ctx, double *ms_per_kind, int *launches_per_kind,
                             gqa_stream_t stream);
 
+/*
+ * attn_decode_attention_noalloc — the decode attention of attn_decode (key/value head
+ * sharing, scores, scaling, softmax over keys 0..kv_len-1, value product, head merge) for
+ * callers that cannot let this library allocate device memory.  The pages have no
+ * counterpart for this entry point: it exists for a serving engine that keeps all of HBM
+ * in its own pool (for example for a paged KV cache) and gives a library only its inputs
+ * and outputs, and for decode loops that cannot afford the device-wide synchronisation a
+ * cudaMalloc implies.  It allocates nothing and needs no context.
+ *
+ * q_r     [B,4096] bf16: rotated queries of the new token of each sequence (what
+ *         attn_debug_buffers returns as q_r after attn_decode).
+ * cache_k, cache_v  [B,S_max,8,128] bf16: rotated keys / values; positions 0..kv_len-1
+ *         are read (the new token's entry must already be written), nothing is written.
+ * h       [B,4096] bf16 output: merged head outputs (the page's H after the merge).
+ * Limits: 1 <= B <= 256, 1 <= kv_len <= S_max <= 1048576; larger B returns GQA_ERR_SHAPE.
+ *
+ * Scratch: the per-split partial results live in one file-scope device array of about
+ * 4.3 MB (2048 units of (sequence, kv head, key split)), which every GPU that loads this
+ * library holds until the process exits.  The first call on a device looks up that
+ * array's device address (cudaGetSymbolAddress) and configures the kernels; make that
+ * first call before any stream capture.  Every call shares the array and it keeps the
+ * last call's contents; calls whose work overlaps on the GPU (other streams or host
+ * threads) race and must be serialised by the caller.  A device-side wait that runs out
+ * is recorded in a status word inside the array, which each call clears first and which
+ * this entry point does not report.
+ * Errors: GQA_ERR_INVALID_ARG, GQA_ERR_SHAPE, GQA_ERR_ALIGN, GQA_ERR_DEVICE (not sm_103),
+ * GQA_ERR_CUDA.
+ */
+gqa_status attn_decode_attention_noalloc(const void *q_r, const void *cache_k,
+                                         const void *cache_v, int B, int kv_len, int S_max,
+                                         void *h, gqa_stream_t stream);
+
 /* attn_destroy — free everything the context owns (after synchronising the device).
  * NULL is ignored. */
 void attn_destroy(gqa_ctx *ctx);

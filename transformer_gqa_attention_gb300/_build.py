@@ -1,6 +1,6 @@
 """Build the in-tree C-ABI library ``libgqa_attn.so`` for sm_103a with nvcc.
 
-Three translation units are compiled in parallel and linked into one shared library
+The translation units are compiled in parallel and linked into one shared library
 (CUDA runtime linked statically, no libcuda link: the driver entry point for tensor-map
 encoding is looked up at run time, so the library also loads on a machine without a GPU).
 """
@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libgqa_attn.so")
 
-SOURCES = ["gqa_abi.cu", "gemm_launch.cu", "attn_launch.cu"]
+SOURCES = ["gqa_abi.cu", "gemm_launch.cu", "attn_launch.cu", "decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

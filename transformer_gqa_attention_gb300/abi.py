@@ -18,8 +18,8 @@ STATUS_NAMES = {0: "GQA_OK", 1: "GQA_ERR_INVALID_ARG", 2: "GQA_ERR_SHAPE", 3: "G
 
 # Every symbol include/gqa_attn.h declares.
 EXPORTED = ("attn_create", "attn_prefill", "attn_decode", "attn_sync_status", "attn_debug_buffers",
-            "attn_profile_begin", "attn_profile_end", "attn_destroy", "attn_strerror",
-            "attn_last_cuda_error")
+            "attn_profile_begin", "attn_profile_end", "attn_decode_attention_noalloc",
+            "attn_destroy", "attn_strerror", "attn_last_cuda_error")
 
 # Kernel kinds of attn_profile_end (GQA_KERNEL_* in include/gqa_attn.h).
 KERNEL_KINDS = ("qkv_gemm", "qkv_splitk", "qkv_finalize", "flash_prefill", "decode_attn",
@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
     L.attn_profile_begin.restype = i32
     L.attn_profile_end.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i32), vp]
     L.attn_profile_end.restype = i32
+    L.attn_decode_attention_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
+    L.attn_decode_attention_noalloc.restype = i32
     L.attn_destroy.argtypes = [vp]
     L.attn_destroy.restype = None
     L.attn_strerror.argtypes = [i32]
@@ -134,6 +136,14 @@ def attn_profile_end(ctx, stream=None):
     cnt = (ctypes.c_int * n)()
     _check("attn_profile_end", lib().attn_profile_end(ctx, ms, cnt, _stream(stream)))
     return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def attn_decode_attention_noalloc(q_r, cache_k, cache_v, B, kv_len, S_max, h, stream=None):
+    """Decode attention into `h` without any device allocation by the library (see the
+    header for the scratch-array limits and the first-call set-up)."""
+    _check("attn_decode_attention_noalloc",
+           lib().attn_decode_attention_noalloc(_ptr(q_r), _ptr(cache_k), _ptr(cache_v), int(B),
+                                               int(kv_len), int(S_max), _ptr(h), _stream(stream)))
 
 
 def attn_destroy(ctx):
