@@ -22,7 +22,7 @@ cudaError_t configure_kernels() {
 
 cudaError_t launch_flash_prefill(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                  const FlashParams& p, dim3 grid, cudaStream_t s) {
-  flash_prefill_kernel<<<grid, 192, FlashSmem::kBytes, s>>>(q, k, v, p);
+  flash_prefill_kernel<<<grid, 384, FlashSmem::kBytes, s>>>(q, k, v, p);
   return cudaGetLastError();
 }
 

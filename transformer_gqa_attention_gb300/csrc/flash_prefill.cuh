@@ -2,18 +2,27 @@
 // "Llama 3.1 8B · Grouped-query attention"): S = Q_r K_G^T, S / sqrt(128), + M, row
 // softmax, H = A V_G, written merged as [B*T, 4096] bf16 (head h at columns 128h..).
 //
-// One CTA = one (sequence b, query head h, 128-query tile).  K_G[h] = K_r[h/4] and
-// V_G[h] = V[h/4] are an index map: the CTA reads kv head g = h/4 of the cache directly.
+// One CTA = one sequence b, one 128-query tile and TWO query heads h0 = 2p, h1 = 2p+1 of
+// the same kv group g = h0/4 (K_G[h] = K_r[h/4], V_G[h] = V[h/4] is an index map: both
+// heads read the same K/V tiles of kv head g from the cache, staged once in shared memory).
+// Both heads have the same causal extent, so they advance through the key tiles together.
 //
-//   warp 0      TMA producer: Q tile once, then 128-key K and V tiles (2 stages each)
-//   warp 1      TMEM owner + UMMA issuer: S_j = Q K_j^T into one of two TMEM S buffers,
-//               then O += P_{j-1} V_{j-1} (P from shared memory, V MN-major)
-//   warps 2..5  softmax: one thread per query row; online softmax in fp32 in the log2
-//               domain with the 1/sqrt(128) scale folded into the exponent; lazy O
-//               rescaling (only when a row max grows by more than 2^8); P written bf16
-//               into the swizzled shared-memory tile the next UMMA reads; final O / l.
+//   warp 0      TMA producer: the two Q tiles once, then 128-key K and V tiles (2 stages)
+//   warp 1      TMEM owner + UMMA issuer.  Per key tile j, for head slot i = 0, 1:
+//                 S_i = Q_i K_j^T (both operands K-major from shared memory) into TMEM,
+//                 O_i += P_i V_j with P_i read from TMEM (it overwrites S_i) and V an
+//                 MN-major shared-memory operand.  Issue order S_0(j+1) before PV_1(j) keeps
+//                 the tensor core busy while the other head's softmax runs.
+//   warps 4..7  softmax of head slot 0, warps 8..11 of head slot 1: one thread per query
+//               row (no shuffles); online softmax in fp32 in the log2 domain with the
+//               1/sqrt(128) scale folded into the exponent; P = exp2(...) rounded to bf16
+//               and stored back into TMEM; lazy per-row rescale of O only when the row max
+//               grows by more than 2^8; final O / l stored to H.
 //
-// TMEM columns: S buffers at 0 and 128, O at 256 (512 allocated).
+// UMMAs issued by one thread complete in order, so the completion of S_i(j) (signalled to
+// the softmax) also means PV_i(j-1) has finished reading P_i(j-1) and writing O_i.
+//
+// TMEM columns: S_0/P_0 at 0, S_1/P_1 at 128, O_0 at 256, O_1 at 384 (512 allocated).
 #pragma once
 
 #include "params.h"
@@ -22,17 +31,16 @@
 namespace gqa {
 
 struct FlashSmem {
-  static constexpr int kTile = 128 * 128 * 2;  // one 128x128 bf16 tile (two 64-col halves)
+  static constexpr int kTile = 128 * 128 * 2;  // one 128x128 bf16 tile (two 64-column halves)
   static constexpr int kHalf = 128 * 64 * 2;
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;          // 2 stages
-  static constexpr int kV = kK + 2 * kTile;      // 2 stages
-  static constexpr int kP = kV + 2 * kTile;
-  static constexpr int kBar = kP + kTile;
+  static constexpr int kQ = 0;                 // 2 tiles (head slots 0, 1)
+  static constexpr int kK = kQ + 2 * kTile;    // 2 stages
+  static constexpr int kV = kK + 2 * kTile;    // 2 stages
+  static constexpr int kBar = kV + 2 * kTile;
   static constexpr int kBytes = kBar + 256 + 1024;
 };
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(384, 1)
     flash_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const FlashParams p) {
   using L = FlashSmem;
@@ -42,24 +50,24 @@ __global__ void __launch_bounds__(192, 1)
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;   // [2]
+  uint64_t* k_full = bars + 1;   // [2] stages
   uint64_t* k_empty = bars + 3;  // [2]
   uint64_t* v_full = bars + 5;   // [2]
   uint64_t* v_empty = bars + 7;  // [2]
-  uint64_t* s_full = bars + 9;   // [2]
-  uint64_t* p_full = bars + 11;
-  uint64_t* o_done = bars + 12;
-  uint64_t* drain = bars + 13;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 14);
+  uint64_t* s_full = bars + 9;   // [2] head slots
+  uint64_t* p_full = bars + 11;  // [2] head slots, 128 arrivals
+  uint64_t* o_full = bars + 13;  // [2] head slots
+  uint64_t* drain = bars + 15;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const int bh = blockIdx.x;
-  const int b = bh / 32;
-  const int h = bh % 32;
-  const int g = h >> 2;
+  const int b = blockIdx.x / 16;
+  const int hp = blockIdx.x % 16;
+  const int h0 = 2 * hp;
+  const int g = h0 >> 2;
   const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.y);  // heaviest tiles first
   const int q0 = qt * 128;
   const int kv_len = p.start_pos + p.T;
@@ -67,7 +75,7 @@ __global__ void __launch_bounds__(192, 1)
   const int n_kv = (kv_hi + 127) / 128;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 14; ++i) mbar_init(&bars[i], i == 11 ? 128u : 1u);  // p_full: 128 rows
+    for (int i = 0; i < 16; ++i) mbar_init(&bars[i], (i == 11 || i == 12) ? 128u : 1u);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -79,7 +87,6 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const uint32_t tmem_O = tmem_base + 256;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -87,10 +94,13 @@ __global__ void __launch_bounds__(192, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(q_full, L::kTile);
-      tma_load_3d(smem + L::kQ, &tmQ, q_full, h * 128, q0, b);
-      tma_load_3d(smem + L::kQ + L::kHalf, &tmQ, q_full, h * 128 + 64, q0, b);
-      int issued = 0;
+      mbar_arrive_expect_tx(q_full, 2 * L::kTile);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        tma_load_3d(smem + L::kQ + i * L::kTile, &tmQ, q_full, (h0 + i) * 128, q0, b);
+        tma_load_3d(smem + L::kQ + i * L::kTile + L::kHalf, &tmQ, q_full, (h0 + i) * 128 + 64, q0, b);
+      }
+      int issued_k = 0, issued_v = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int st = j & 1;
         const uint32_t ph = (j >> 1) & 1;
@@ -99,65 +109,85 @@ __global__ void __launch_bounds__(192, 1)
         uint8_t* kd = smem + L::kK + st * L::kTile;
         tma_load_4d(kd, &tmK, &k_full[st], 0, g, j * 128, b);
         tma_load_4d(kd + L::kHalf, &tmK, &k_full[st], 64, g, j * 128, b);
-        if (!mbar_wait(&v_empty[st], ph ^ 1u, abort_flag, p.status)) { ++issued; break; }
+        ++issued_k;
+        if (!mbar_wait(&v_empty[st], ph ^ 1u, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(&v_full[st], L::kTile);
         uint8_t* vd = smem + L::kV + st * L::kTile;
         tma_load_4d(vd, &tmV, &v_full[st], 0, g, j * 128, b);
         tma_load_4d(vd + L::kHalf, &tmV, &v_full[st], 64, g, j * 128, b);
-        ++issued;
+        ++issued_v;
       }
-      if (*abort_flag) {
+      if (*abort_flag) {  // let copies still in flight land before the CTA leaves
         mbar_wait_drain(q_full, 0);
-        for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) {
+        for (int j = (issued_k > 2 ? issued_k - 2 : 0); j < issued_k; ++j)
           mbar_wait_drain(&k_full[j & 1], (j >> 1) & 1);
+        for (int j = (issued_v > 2 ? issued_v - 2 : 0); j < issued_v; ++j)
           mbar_wait_drain(&v_full[j & 1], (j >> 1) & 1);
-        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------------- UMMA issuer
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);   // Q, K both K-major
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, 0, 1);  // P K-major, V MN-major
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, 0, 1);  // P (TMEM), V MN-major
       const uint32_t q_addr = smem_u32(smem + L::kQ);
       const uint32_t k_addr = smem_u32(smem + L::kK);
       const uint32_t v_addr = smem_u32(smem + L::kV);
-      const uint32_t p_addr = smem_u32(smem + L::kP);
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
-      for (int j = 0; ok && j <= n_kv; ++j) {
-        if (j < n_kv) {
-          const int st = j & 1;
-          if (!mbar_wait(&k_full[st], (j >> 1) & 1, abort_flag, p.status)) break;
-          tc_fence_after();
-          const uint32_t d_s = tmem_base + st * 128;
+      // S_i(j) = Q_i K_j^T
+      auto issue_s = [&](int i, int j) {
+        const int st = j & 1;
+        const uint32_t d_s = tmem_base + i * 128;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * L::kHalf + (kk & 3) * 32;
-            umma_ss(d_s, sdesc_sw128(q_addr + off, 0, 1024),
-                    sdesc_sw128(k_addr + st * L::kTile + off, 0, 1024), idesc_s, kk != 0);
-          }
-          umma_commit(&k_empty[st]);
-          umma_commit(&s_full[st]);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kHalf + (kk & 3) * 32;
+          umma_ss(d_s, sdesc_sw128(q_addr + i * L::kTile + off, 0, 1024),
+                  sdesc_sw128(k_addr + st * L::kTile + off, 0, 1024), idesc_s, kk != 0);
         }
-        if (j >= 1) {
-          const int jp = j - 1;
-          const int st = jp & 1;
-          if (!mbar_wait(p_full, jp & 1, abort_flag, p.status)) break;
-          if (!mbar_wait(&v_full[st], (jp >> 1) & 1, abort_flag, p.status)) break;
-          tc_fence_after();
+        umma_commit(&s_full[i]);
+      };
+      // O_i += P_i(j) V_j; P_i holds keys (2c, 2c+1) in column c of S_i's TMEM columns.
+      auto issue_pv = [&](int i, int j) {
+        const int st = j & 1;
+        const uint32_t d_o = tmem_base + 256 + i * 128;
+        const uint32_t a_p = tmem_base + i * 128;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            // P: K-major, keys 16kk..16kk+15 -> half kk/4, +32 B per step inside the atom.
-            const uint32_t poff = (kk >> 2) * L::kHalf + (kk & 3) * 32;
-            // V: MN-major (d contiguous); 16 keys = two 8-row groups = 2048 B per step;
-            // d 64..127 lives in the second half (LBO), 8-key groups 1024 B apart (SBO).
-            const uint32_t voff = kk * 2048;
-            umma_ss(tmem_O, sdesc_sw128(p_addr + poff, 0, 1024),
-                    sdesc_sw128(v_addr + st * L::kTile + voff, L::kHalf, 1024), idesc_pv,
-                    (jp | kk) != 0);
-          }
-          umma_commit(&v_empty[st]);
-          umma_commit(o_done);
+        for (int kk = 0; kk < 8; ++kk) {
+          // V: MN-major (d contiguous); 16 keys = two 8-row groups = 2048 B per step;
+          // d 64..127 lives in the second half (LBO), 8-key groups 1024 B apart (SBO).
+          umma_ts(d_o, a_p + kk * 8, sdesc_sw128(v_addr + st * L::kTile + kk * 2048, L::kHalf, 1024),
+                  idesc_pv, (j | kk) != 0);
+        }
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
+      if (ok) ok = mbar_wait(&k_full[0], 0, abort_flag, p.status);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+        umma_commit(&k_empty[0]);
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const bool more = j + 1 < n_kv;
+        // head slot 0: PV_0(j), then S_0(j+1)
+        if (!(ok = mbar_wait(&v_full[j & 1], (j >> 1) & 1, abort_flag, p.status))) break;
+        if (!(ok = mbar_wait(&p_full[0], j & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        issue_pv(0, j);
+        if (!more) umma_commit(&o_full[0]);
+        if (more) {
+          if (!(ok = mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+          issue_s(0, j + 1);
+        }
+        // head slot 1: PV_1(j), then S_1(j+1)
+        if (!(ok = mbar_wait(&p_full[1], j & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        issue_pv(1, j);
+        umma_commit(&v_empty[j & 1]);
+        if (!more) umma_commit(&o_full[1]);
+        if (more) {
+          issue_s(1, j + 1);
+          umma_commit(&k_empty[(j + 1) & 1]);
         }
       }
       if (*abort_flag) {  // let issued UMMAs finish before TMEM is released
@@ -165,27 +195,27 @@ __global__ void __launch_bounds__(192, 1)
         mbar_wait_drain(drain, 0);
       }
     }
-  } else {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax
+    const int slot = (warp - 4) >> 2;  // head slot 0 or 1
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // query row inside the tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem_base + lane_off + slot * 128;
+    const uint32_t t_o = tmem_base + lane_off + 256 + slot * 128;
     const int qpos = p.start_pos + q0 + r;
-    uint8_t* Ps = smem + L::kP;
     float m_used = -INFINITY;
     float l_sum = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      const int st = j & 1;
-      ok = mbar_wait(&s_full[st], (j >> 1) & 1, abort_flag, p.status);
-      ok = __all_sync(0xffffffffu, ok);
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[slot], j & 1, abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();
       float s[128];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem_base + lane_off + st * 128 + c * 32, v);
+        tmem_ld32(t_s + c * 32, v);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
@@ -202,76 +232,60 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int i = 0; i < 128; ++i) mx = fmaxf(mx, s[i]);
       const float m_tile = mx * p.scale_log2;
-      // PV_{j-1} must be complete before O is rescaled and before P is overwritten.
-      if (j >= 1) {
-        ok = mbar_wait(o_done, (j - 1) & 1, abort_flag, p.status);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
-      }
+      // Per-row lazy rescale decision (rows never influence each other's bits).
+      float alpha = 1.f;
+      bool grow = false;
       if (j == 0) {
         m_used = m_tile;
-      } else {
-        // Per-row decision (rows never influence each other's bits); the TMEM round trip is
-        // warp-collective, rows that keep their max scale by exactly 1.
-        const bool grow = m_tile > m_used + 8.0f;
-        if (__any_sync(0xffffffffu, grow)) {
-          float alpha = 1.f;
-          if (grow) {
-            alpha = fast_exp2(m_used - m_tile);
-            l_sum *= alpha;
-            m_used = m_tile;
-          }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tmem_O + lane_off + c * 32, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st32(tmem_O + lane_off + c * 32, v);
-          }
-          tmem_st_wait();
-        }
+      } else if (m_tile > m_used + 8.0f) {
+        grow = true;
+        alpha = fast_exp2(m_used - m_tile);
+        l_sum *= alpha;
+        m_used = m_tile;
       }
       const float mu = (m_used == -INFINITY) ? 0.f : m_used;
-      // P = exp2(s * scale_log2 - m_used), written bf16 into the swizzled P tile.
+      // P = exp2(s * scale_log2 - m_used), bf16, written over S_i in TMEM.
       float lsum = 0.f;
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint8_t* prow = Ps + hf * L::kHalf + (r >> 3) * 1024 + (r & 7) * 128;
+      for (int c = 0; c < 4; ++c) {
+        uint32_t w[16];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = hf * 64 + c * 8 + 2 * e;
-            const float p0 = fast_exp2(fmaf(s[i], p.scale_log2, -mu));
-            const float p1 = fast_exp2(fmaf(s[i + 1], p.scale_log2, -mu));
-            lsum += p0 + p1;
-            w[e] = pack_bf16x2(p0, p1);
-          }
-          *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = fast_exp2(fmaf(s[c * 32 + 2 * e], p.scale_log2, -mu));
+          const float p1 = fast_exp2(fmaf(s[c * 32 + 2 * e + 1], p.scale_log2, -mu));
+          lsum += p0 + p1;
+          w[e] = pack_bf16x2(p0, p1);
         }
+        tmem_st16(t_s + c * 16, w);
       }
       l_sum += lsum;
-      fence_proxy_async_smem();
+      // O_i holds the sum through key tile j-1 (PV_i(j-1) completed before S_i(j)).
+      if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(t_o + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+          tmem_st32(t_o + c * 32, v);
+        }
+      }
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[slot]);
     }
-    if (ok) {
-      ok = mbar_wait(o_done, (n_kv - 1) & 1, abort_flag, p.status);
-      ok = __all_sync(0xffffffffu, ok);
-    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[slot], 0, abort_flag, p.status));
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l_sum;
       const bool valid = (q0 + r) < p.T;
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.H) + (static_cast<size_t>(b) * p.T + q0 + r) * 4096 + h * 128;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.H) + (static_cast<size_t>(b) * p.T + q0 + r) * 4096 +
+                           (h0 + slot) * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem_O + lane_off + c * 32, v);
+        tmem_ld32(t_o + c * 32, v);
         tmem_ld_wait();
         if (valid) {
           uint32_t w[16];

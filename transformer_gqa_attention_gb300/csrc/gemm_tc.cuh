@@ -1,12 +1,19 @@
-// gemm_tc.cuh — warp-specialised tcgen05 GEMM, D[M,N] = A[M,K] * B[N,K]^T, both operands
-// K-major bf16 (the [out, in] weight storage of the quoted F.linear layers), fp32
-// accumulation in TMEM.
+// gemm_tc.cuh — persistent, warp-specialised tcgen05 GEMM, D[M,N] = A[M,K] * B[N,K]^T,
+// both operands K-major bf16 (the [out, in] weight storage of the quoted F.linear
+// layers), fp32 accumulation in TMEM.
 //
-//   warp 0      TMA producer: 128x64 A box + BNx64 B box per stage, 128-byte swizzle
+//   warp 0      TMA producer: 128x64 A box + BNx64 B box per stage, 128-byte swizzle,
+//               one stage ring shared by all the CTA's work units
 //   warp 1      TMEM owner + single-thread UMMA issuer (128 x BN x 16 per instruction)
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows, fused output transform
+//               into one of two TMEM accumulators (2 x BN columns)
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows, fused output transform;
+//               while it drains one accumulator the issuer fills the other, so the
+//               epilogue of unit i runs under the main loop of unit i+1
 //
-// Epilogues (one output tile per CTA):
+// Work units (m tile, n tile, k split) are numbered with the n tile fastest, so the CTAs
+// resident at one time share A row bands through L2; CTA c takes units c, c+G, c+2G, ...
+//
+// Epilogues:
 //   kQkvRope  — the fused Q/K/V projection (steps 1-5 of "Llama 3.1 8B · Grouped-query
 //               attention"): columns 0..4095 are Q, 4096..5119 K, 5120..6143 V of the
 //               packed [6144,4096] weight.  Q and K pairs (2j, 2j+1) are rotated by
@@ -30,7 +37,73 @@ struct GemmSmem {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kBarOffset = STAGES * kStageBytes;
   static constexpr int kBytes = kBarOffset + 256 + 1024;  // + barriers + alignment slack
+  static constexpr int kTmemCols = 2 * BN;                // two accumulators
 };
+
+struct GemmUnit {
+  int m0, n0, split, kb0, nkb;
+};
+
+__device__ __forceinline__ GemmUnit gemm_unit(const GemmParams& p, int u, int BN) {
+  GemmUnit w;
+  w.split = u % p.splits;
+  const int tile = u / p.splits;
+  w.n0 = (tile % p.n_tiles) * BN;
+  w.m0 = (tile / p.n_tiles) * 128;
+  w.kb0 = w.split * p.kb_per_split;
+  w.nkb = (w.split == p.splits - 1) ? (p.num_kb - w.kb0) : p.kb_per_split;
+  return w;
+}
+
+// Transform and store 32 accumulator columns (col0 .. col0+31) of output row m.
+template <int EPI>
+__device__ __forceinline__ void gemm_epilogue_chunk(const GemmParams& p, int m, int col0, int split,
+                                                    const uint32_t (&v)[32]) {
+  if (m >= p.M) return;
+  if constexpr (EPI == kQkvRope) {
+    const int b = m / p.T;
+    const int t = m - b * p.T;
+    const bool is_v = col0 >= 5120;
+    uint32_t w[16];
+    if (is_v) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+    } else {
+      // pairs j0 .. j0+15 of this head slice
+      const int j0 = (col0 & 127) >> 1;
+      const float4* rp = reinterpret_cast<const float4*>(p.R + (static_cast<size_t>(t) * 64 + j0) * 2);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 cs = __ldg(rp + i);  // (cos, sin) of pairs 2i and 2i+1
+        const float e0 = __uint_as_float(v[4 * i + 0]), o0 = __uint_as_float(v[4 * i + 1]);
+        const float e1 = __uint_as_float(v[4 * i + 2]), o1 = __uint_as_float(v[4 * i + 3]);
+        w[2 * i + 0] = pack_bf16x2(cs.x * e0 - cs.y * o0, cs.y * e0 + cs.x * o0);
+        w[2 * i + 1] = pack_bf16x2(cs.z * e1 - cs.w * o1, cs.w * e1 + cs.z * o1);
+      }
+    }
+    __nv_bfloat16* dst;
+    if (col0 < 4096) {
+      dst = static_cast<__nv_bfloat16*>(p.out0) + static_cast<size_t>(m) * 4096 + col0;
+    } else {
+      const size_t cache_row = static_cast<size_t>(b) * p.S_max + p.start_pos + t;
+      dst = static_cast<__nv_bfloat16*>(is_v ? p.out2 : p.out1) + cache_row * 1024 + (col0 - (is_v ? 5120 : 4096));
+    }
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  } else if constexpr (EPI == kStoreF32) {
+    float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(p.out0) + static_cast<size_t>(m) * p.ldo + col0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                          __uint_as_float(v[4 * i + 3]));
+  } else {  // kPartialT: slab [split][token][feature]; a warp stores 32 consecutive features
+    float* base = static_cast<float*>(p.out0) + static_cast<size_t>(split) * p.slab +
+                  static_cast<size_t>(col0) * p.ldo + m;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) base[static_cast<size_t>(i) * p.ldo] = __uint_as_float(v[i]);
+  }
+}
 
 template <int BN, int STAGES, int EPI>
 __global__ void __launch_bounds__(192, 1)
@@ -45,33 +118,31 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* sB = smem + STAGES * L::kABytes;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
   uint64_t* empty_bar = full_bar + STAGES;
-  uint64_t* acc_bar = empty_bar + STAGES;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_bar + 1);
+  uint64_t* acc_full = empty_bar + STAGES;  // [2]
+  uint64_t* acc_empty = acc_full + 2;       // [2]
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  const int split = blockIdx.x % p.splits;
-  const int tile = blockIdx.x / p.splits;
-  const int n_tile = tile % p.n_tiles;
-  const int m_tile = tile / p.n_tiles;
-  const int m0 = m_tile * 128;
-  const int n0 = n_tile * BN;
-  const int kb0 = split * p.kb_per_split;
-  const int nkb = (split == p.splits - 1) ? (p.num_kb - kb0) : p.kb_per_split;
+  const int total_units = p.m_tiles * p.n_tiles * p.splits;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(acc_bar, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 128);
+    }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, BN);
+    tmem_alloc(tmem_holder, L::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -84,19 +155,25 @@ __global__ void __launch_bounds__(192, 1)
       // ------------------------------------------------------------ TMA producer
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
-      int issued = 0;
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % STAGES;
-        const uint32_t ph = (i / STAGES) & 1;
-        if (!mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&full_bar[s], L::kStageBytes);
-        const int kc = (kb0 + i) * 64;
-        tma_load_2d(sA + s * L::kABytes, &tmA, &full_bar[s], kc, m0);
-        tma_load_2d(sB + s * L::kBBytes, &tmB, &full_bar[s], kc, n0);
-        ++issued;
+      int it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const GemmUnit w = gemm_unit(p, u, BN);
+        for (int i = 0; i < w.nkb; ++i, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[s], L::kStageBytes);
+          const int kc = (w.kb0 + i) * 64;
+          tma_load_2d(sA + s * L::kABytes, &tmA, &full_bar[s], kc, w.m0);
+          tma_load_2d(sB + s * L::kBBytes, &tmB, &full_bar[s], kc, w.n0);
+        }
       }
       if (*abort_flag) {  // let copies still in flight land before the CTA leaves
-        for (int i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
+        for (int i = (it > STAGES ? it - STAGES : 0); i < it; ++i)
           mbar_wait_drain(&full_bar[i % STAGES], (i / STAGES) & 1);
       }
     }
@@ -106,89 +183,60 @@ __global__ void __launch_bounds__(192, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(128, BN, 0, 0);
       const uint32_t a_base = smem_u32(sA);
       const uint32_t b_base = smem_u32(sB);
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % STAGES;
-        const uint32_t ph = (i / STAGES) & 1;
-        if (!mbar_wait(&full_bar[s], ph, abort_flag, p.status)) break;
+      int it = 0, lt = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++lt) {
+        const GemmUnit w = gemm_unit(p, u, BN);
+        const int ab = lt & 1;
+        if (!mbar_wait(&acc_empty[ab], ((lt >> 1) & 1) ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
+        const uint32_t d_tmem = tmem_base + ab * BN;
+        for (int i = 0; i < w.nkb; ++i, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(&full_bar[s], ph, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t da = sdesc_sw128(a_base + s * L::kABytes + k * 32, 0, 1024);
-          const uint64_t db = sdesc_sw128(b_base + s * L::kBBytes + k * 32, 0, 1024);
-          umma_ss(tmem_base, da, db, idesc, (i | k) != 0);
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t da = sdesc_sw128(a_base + s * L::kABytes + k * 32, 0, 1024);
+            const uint64_t db = sdesc_sw128(b_base + s * L::kBBytes + k * 32, 0, 1024);
+            umma_ss(d_tmem, da, db, idesc, (i | k) != 0);
+          }
+          umma_commit(&empty_bar[s]);
         }
-        umma_commit(&empty_bar[s]);
+        if (ok) umma_commit(&acc_full[ab]);
       }
-      umma_commit(acc_bar);
-      if (*abort_flag) mbar_wait_drain(acc_bar, 0);
+      if (*abort_flag) {  // let issued UMMAs finish before TMEM is released
+        umma_commit(drain);
+        mbar_wait_drain(drain, 0);
+      }
     }
   } else {
     // -------------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_bar, 0, abort_flag, p.status));
-    tc_fence_after();
-    if (ok) {
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-      const int m = m0 + row;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    int lt = 0;
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++lt) {
+      const GemmUnit w = gemm_unit(p, u, BN);
+      const int ab = lt & 1;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[ab], (lt >> 1) & 1, abort_flag, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + lane_off + ab * BN;
+      const int m = w.m0 + row;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(t_row + c * 32, v);
         tmem_ld_wait();
-        const int col0 = n0 + c * 32;
-        if constexpr (EPI == kQkvRope) {
-          if (m < p.M) {
-            const int b = m / p.T;
-            const int t = m - b * p.T;
-            const bool is_v = col0 >= 5120;
-            uint32_t w[16];
-            if (is_v) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                w[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-            } else {
-              // pairs j0 .. j0+15 of this head slice
-              const int j0 = (col0 & 127) >> 1;
-              const float4* rp = reinterpret_cast<const float4*>(p.R + (static_cast<size_t>(t) * 64 + j0) * 2);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float4 cs = __ldg(rp + i);  // (cos, sin) of pairs 2i and 2i+1
-                const float e0 = __uint_as_float(v[4 * i + 0]), o0 = __uint_as_float(v[4 * i + 1]);
-                const float e1 = __uint_as_float(v[4 * i + 2]), o1 = __uint_as_float(v[4 * i + 3]);
-                w[2 * i + 0] = pack_bf16x2(cs.x * e0 - cs.y * o0, cs.y * e0 + cs.x * o0);
-                w[2 * i + 1] = pack_bf16x2(cs.z * e1 - cs.w * o1, cs.w * e1 + cs.z * o1);
-              }
-            }
-            __nv_bfloat16* dst;
-            if (col0 < 4096) {
-              dst = static_cast<__nv_bfloat16*>(p.out0) + static_cast<size_t>(m) * 4096 + col0;
-            } else {
-              const size_t cache_row = static_cast<size_t>(b) * p.S_max + p.start_pos + t;
-              dst = static_cast<__nv_bfloat16*>(is_v ? p.out2 : p.out1) + cache_row * 1024 +
-                    (col0 - (is_v ? 5120 : 4096));
-            }
-            uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-          }
-        } else if constexpr (EPI == kStoreF32) {
-          if (m < p.M) {
-            float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(p.out0) + static_cast<size_t>(m) * p.ldo + col0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-          }
-        } else {  // kPartialT: slab [split][token][feature]; a warp stores 32 consecutive features
-          if (m < p.M) {
-            float* base = static_cast<float*>(p.out0) + static_cast<size_t>(split) * p.slab +
-                          static_cast<size_t>(col0) * p.ldo + m;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) base[static_cast<size_t>(i) * p.ldo] = __uint_as_float(v[i]);
-          }
-        }
+        gemm_epilogue_chunk<EPI>(p, m, w.n0 + c * 32, w.split, v);
       }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[ab]);
     }
   }
 
@@ -196,7 +244,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, BN);
+    tmem_dealloc(tmem_base, L::kTmemCols);
   }
 }
 

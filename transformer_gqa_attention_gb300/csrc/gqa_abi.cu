@@ -247,10 +247,11 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
     p.splits = sk->splits_qkv;
     p.kb_per_split = 64 / p.splits;
     p.n_tiles = sk->n_tiles;
+    p.m_tiles = 48;
     p.out0 = c->ws + w.part_off;
     p.ldo = 6144;
     p.slab = static_cast<long long>(sk->tok_pad) * 6144;
-    const int grid = 48 * p.n_tiles * p.splits;
+    const int grid = std::min(p.m_tiles * p.n_tiles * p.splits, 2 * c->num_sms);
     { ProfScope ps(c, GQA_KERNEL_QKV_SPLITK, s); GQA_CUDA(launch_gemm_partial(ta, tb, p, grid, s)); }
     QkvFinalizeParams f{};
     f.part = reinterpret_cast<const float*>(c->ws + w.part_off);
@@ -273,11 +274,12 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
     p.splits = 1;
     p.kb_per_split = 64;
     p.n_tiles = 24;
+    p.m_tiles = (n_tok + 127) / 128;
     p.out0 = q_out;
     p.out1 = ck;
     p.out2 = cv;
     p.R = R;
-    const int grid = ((n_tok + 127) / 128) * 24;
+    const int grid = std::min(p.m_tiles * p.n_tiles, c->num_sms);
     { ProfScope ps(c, GQA_KERNEL_QKV_GEMM, s); GQA_CUDA(launch_gemm_qkv_rope(ta, tb, p, grid, s)); }
   }
   return GQA_OK;
@@ -298,10 +300,12 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
     p.splits = sk->splits_o;
     p.kb_per_split = 64 / p.splits;
     p.n_tiles = sk->n_tiles;
+    p.m_tiles = 32;
     p.out0 = c->ws + w.part_off;
     p.ldo = 4096;
     p.slab = static_cast<long long>(sk->tok_pad) * 4096;
-    { ProfScope ps(c, GQA_KERNEL_OUT_SPLITK, s); GQA_CUDA(launch_gemm_partial(ta, tb, p, 32 * p.n_tiles * p.splits, s)); }
+    const int grid = std::min(p.m_tiles * p.n_tiles * p.splits, 2 * c->num_sms);
+    { ProfScope ps(c, GQA_KERNEL_OUT_SPLITK, s); GQA_CUDA(launch_gemm_partial(ta, tb, p, grid, s)); }
     OutFinalizeParams f{};
     f.part = reinterpret_cast<const float*>(c->ws + w.part_off);
     f.slab = p.slab;
@@ -317,9 +321,11 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
     p.splits = 1;
     p.kb_per_split = 64;
     p.n_tiles = 16;
+    p.m_tiles = (n_tok + 127) / 128;
     p.out0 = delta;
     p.ldo = 4096;
-    { ProfScope ps(c, GQA_KERNEL_OUT_GEMM, s); GQA_CUDA(launch_gemm_store_f32(ta, tb, p, ((n_tok + 127) / 128) * 16, s)); }
+    const int grid = std::min(p.m_tiles * p.n_tiles, c->num_sms);
+    { ProfScope ps(c, GQA_KERNEL_OUT_GEMM, s); GQA_CUDA(launch_gemm_store_f32(ta, tb, p, grid, s)); }
   }
   return GQA_OK;
 }
@@ -433,7 +439,7 @@ gqa_status attn_prefill(gqa_ctx* c, const void* x, int B, int T, const float* R,
   fp.H = h;
   fp.status = c->status;
   fp.scale_log2 = kScaleLog2;
-  { ProfScope ps(c, GQA_KERNEL_FLASH_PREFILL, s); GQA_CUDA(launch_flash_prefill(tq, tk, tv, fp, dim3(B * 32, fp.n_qtiles), s)); }
+  { ProfScope ps(c, GQA_KERNEL_FLASH_PREFILL, s); GQA_CUDA(launch_flash_prefill(tq, tk, tv, fp, dim3(B * 16, fp.n_qtiles), s)); }
 
   return run_out(c, h, n_tok, delta, w, sk, s);
 }

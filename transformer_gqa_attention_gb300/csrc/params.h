@@ -21,6 +21,7 @@ struct GemmParams {
   int kb_per_split;  // k-blocks per split (last split takes the remainder)
   int splits;
   int n_tiles;       // ceil(N / BN)
+  int m_tiles;       // ceil(M / 128)
   // epilogue operands
   void* out0;        // kQkvRope: Q_r [M,4096] bf16 | kStoreF32: D fp32 | kPartialT: partial base
   void* out1;        // kQkvRope: cache_k
