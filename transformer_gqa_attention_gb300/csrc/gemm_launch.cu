@@ -5,33 +5,46 @@
 
 namespace gqa {
 
-using WideSmem = GemmSmem<256, 4>;
+using PairSmem = GemmPairSmem<6>;
 using SkinnySmem = GemmSmem<64, 4>;
 
-size_t gemm_wide_smem() { return WideSmem::kBytes; }
+size_t gemm_wide_smem() { return PairSmem::kBytes; }
 size_t gemm_skinny_smem() { return SkinnySmem::kBytes; }
 
 cudaError_t configure_gemm_kernels() {
   cudaError_t e;
-  e = cudaFuncSetAttribute(gemm_tc_kernel<256, 4, kQkvRope>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           WideSmem::kBytes);
+  e = cudaFuncSetAttribute(gemm_tc_pair_kernel<6, kQkvRope>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           PairSmem::kBytes);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(gemm_tc_kernel<256, 4, kStoreF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           WideSmem::kBytes);
+  e = cudaFuncSetAttribute(gemm_tc_pair_kernel<6, kStoreF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           PairSmem::kBytes);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(gemm_tc_kernel<64, 4, kPartialT>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, SkinnySmem::kBytes);
 }
 
+int gemm_pair_max_clusters() {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = PairSmem::kBytes;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_pair_kernel<6, kQkvRope>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
 cudaError_t launch_gemm_qkv_rope(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                                  int grid, cudaStream_t s) {
-  gemm_tc_kernel<256, 4, kQkvRope><<<grid, 192, WideSmem::kBytes, s>>>(a, b, p);
+  gemm_tc_pair_kernel<6, kQkvRope><<<grid, 192, PairSmem::kBytes, s>>>(a, b, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_store_f32(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                                   int grid, cudaStream_t s) {
-  gemm_tc_kernel<256, 4, kStoreF32><<<grid, 192, WideSmem::kBytes, s>>>(a, b, p);
+  gemm_tc_pair_kernel<6, kStoreF32><<<grid, 192, PairSmem::kBytes, s>>>(a, b, p);
   return cudaGetLastError();
 }
 

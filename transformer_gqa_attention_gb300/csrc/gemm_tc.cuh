@@ -248,4 +248,174 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// CTA-pair variant (cta_group::2) for the many-token projections: a cluster of two CTAs
+// computes one 256x256 output tile.  CTA r stages its own 128 rows of A (rows m0+128r..)
+// and its own 128 rows of B (rows n0+128r.., i.e. half of the tile's N) per 64-wide k
+// block; the single issuing thread in CTA 0 runs 256x256x16 UMMAs that read both CTAs'
+// shared memory and leave each CTA's 128 output rows (all 256 columns) in its own TMEM.
+// Per CTA a stage is 32 KB instead of 48 KB for a 128x256 single-CTA tile, so six stages
+// fit and each SM streams half as many B bytes per FLOP.
+//   - both CTAs' TMA loads complete on CTA 0's full barrier (CTA 0 expects both halves);
+//   - CTA 0's commits arrive on the empty / accumulator-full barriers of both CTAs;
+//   - each CTA's epilogue warps release an accumulator on CTA 0's acc_empty barrier.
+template <int STAGES>
+struct GemmPairSmem {
+  static constexpr int kABytes = 128 * 64 * 2;
+  static constexpr int kBBytes = 128 * 64 * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kBarOffset = STAGES * kStageBytes;
+  static constexpr int kBytes = kBarOffset + 256 + 1024;
+  static constexpr int kTmemCols = 512;  // two 256-column accumulators
+};
+
+template <int STAGES, int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const GemmParams p) {
+  using L = GemmPairSmem<STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * L::kABytes;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* acc_full = empty_bar + STAGES;  // [2]
+  uint64_t* acc_empty = acc_full + 2;       // [2], used in CTA 0 only
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1;
+  const int n_pairs = gridDim.x >> 1;
+  const int total_units = p.m_tiles * p.n_tiles;  // 256x256 tiles, n fastest
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 8);  // one arrival per epilogue warp of both CTAs
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_holder, L::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // peer barriers initialised before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int it = 0;
+      bool ok = true;
+      for (int u = pair; ok && u < total_units; u += n_pairs) {
+        const int m0 = (u / p.n_tiles) * 256 + 128 * rank;
+        const int n0 = (u % p.n_tiles) * 256 + 128 * rank;
+        for (int i = 0; i < p.num_kb; ++i, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * L::kStageBytes);
+          const uint32_t bar0 = mapa_shared(smem_u32(&full_bar[s]), 0);
+          tma_load_2d_pair(sA + s * L::kABytes, &tmA, bar0, i * 64, m0);
+          tma_load_2d_pair(sB + s * L::kBBytes, &tmB, bar0, i * 64, n0);
+        }
+      }
+      if (*abort_flag && rank == 0) {  // CTA 0's barriers count both CTAs' bytes
+        for (int i = (it > STAGES ? it - STAGES : 0); i < it; ++i)
+          mbar_wait_drain(&full_bar[i % STAGES], (i / STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ------------------------------------------------------------ UMMA issuer (CTA 0)
+      constexpr uint32_t idesc = idesc_bf16_f32(256, 256, 0, 0);
+      const uint32_t a_base = smem_u32(sA);
+      const uint32_t b_base = smem_u32(sB);
+      int it = 0, lt = 0;
+      bool ok = true;
+      for (int u = pair; ok && u < total_units; u += n_pairs, ++lt) {
+        const int ab = lt & 1;
+        if (!mbar_wait(&acc_empty[ab], ((lt >> 1) & 1) ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + ab * 256;
+        for (int i = 0; i < p.num_kb; ++i, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(&full_bar[s], ph, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t da = sdesc_sw128(a_base + s * L::kABytes + k * 32, 0, 1024);
+            const uint64_t db = sdesc_sw128(b_base + s * L::kBBytes + k * 32, 0, 1024);
+            umma_ss_pair(d_tmem, da, db, idesc, (i | k) != 0);
+          }
+          umma_commit_pair(&empty_bar[s], 0x3);
+        }
+        if (ok) umma_commit_pair(&acc_full[ab], 0x3);
+      }
+      if (*abort_flag) {  // let issued UMMAs finish before TMEM is released
+        umma_commit_pair(drain, 0x1);
+        mbar_wait_drain(drain, 0);
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    int lt = 0;
+    for (int u = pair; u < total_units; u += n_pairs, ++lt) {
+      const int ab = lt & 1;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[ab], (lt >> 1) & 1, abort_flag, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + lane_off + ab * 256;
+      const int m = (u / p.n_tiles) * 256 + 128 * rank + row;
+      const int n0 = (u % p.n_tiles) * 256;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t v[32];
+        tmem_ld32(t_row + c * 32, v);
+        tmem_ld_wait();
+        gemm_epilogue_chunk<EPI>(p, m, n0 + c * 32, 0, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[ab]), 0));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the pair's UMMAs or remote arrivals are live
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, L::kTmemCols);
+  }
+}
+
 }  // namespace gqa

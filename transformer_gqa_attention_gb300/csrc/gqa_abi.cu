@@ -21,6 +21,7 @@ using namespace gqa;
 struct gqa_ctx {
   int device = -1;
   int num_sms = 0;
+  int pair_clusters = 0;  // co-resident 2-CTA clusters of the pair GEMM
   __nv_bfloat16* w_qkv = nullptr;  // [6144, 4096]: W_Q rows 0..4095, W_K 4096..5119, W_V 5120..6143
   __nv_bfloat16* w_o = nullptr;    // [4096, 4096]
   int* status = nullptr;           // device status word (kDevErr* bits)
@@ -267,19 +268,20 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
     f.cache_v = cv;
     { ProfScope ps(c, GQA_KERNEL_QKV_FINALIZE, s); GQA_CUDA(launch_qkv_finalize(f, s)); }
   } else {
-    if (!map_rows_k4096(&ta, x, n_tok, 128) || !map_rows_k4096(&tb, c->w_qkv, 6144, 256))
+    // CTA pairs, 256x256 tiles: each CTA loads 128-row boxes of x and of W_QKV
+    if (!map_rows_k4096(&ta, x, n_tok, 128) || !map_rows_k4096(&tb, c->w_qkv, 6144, 128))
       return cuda_fail(cudaErrorInvalidValue);
     p.M = n_tok;
     p.N = 6144;
     p.splits = 1;
     p.kb_per_split = 64;
     p.n_tiles = 24;
-    p.m_tiles = (n_tok + 127) / 128;
+    p.m_tiles = (n_tok + 255) / 256;
     p.out0 = q_out;
     p.out1 = ck;
     p.out2 = cv;
     p.R = R;
-    const int grid = std::min(p.m_tiles * p.n_tiles, c->num_sms);
+    const int grid = 2 * std::min(p.m_tiles * p.n_tiles, c->pair_clusters);
     { ProfScope ps(c, GQA_KERNEL_QKV_GEMM, s); GQA_CUDA(launch_gemm_qkv_rope(ta, tb, p, grid, s)); }
   }
   return GQA_OK;
@@ -314,17 +316,17 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
     f.delta = delta;
     { ProfScope ps(c, GQA_KERNEL_OUT_FINALIZE, s); GQA_CUDA(launch_out_finalize(f, s)); }
   } else {
-    if (!map_rows_k4096(&ta, h, n_tok, 128) || !map_rows_k4096(&tb, c->w_o, 4096, 256))
+    if (!map_rows_k4096(&ta, h, n_tok, 128) || !map_rows_k4096(&tb, c->w_o, 4096, 128))
       return cuda_fail(cudaErrorInvalidValue);
     p.M = n_tok;
     p.N = 4096;
     p.splits = 1;
     p.kb_per_split = 64;
     p.n_tiles = 16;
-    p.m_tiles = (n_tok + 127) / 128;
+    p.m_tiles = (n_tok + 255) / 256;
     p.out0 = delta;
     p.ldo = 4096;
-    const int grid = std::min(p.m_tiles * p.n_tiles, c->num_sms);
+    const int grid = 2 * std::min(p.m_tiles * p.n_tiles, c->pair_clusters);
     { ProfScope ps(c, GQA_KERNEL_OUT_GEMM, s); GQA_CUDA(launch_gemm_store_f32(ta, tb, p, grid, s)); }
   }
   return GQA_OK;
@@ -367,6 +369,8 @@ gqa_status attn_create(const void* wq, const void* wk, const void* wv, const voi
   gqa_ctx* c = new gqa_ctx();
   c->device = dev;
   c->num_sms = prop.multiProcessorCount;
+  c->pair_clusters = gemm_pair_max_clusters();
+  if (c->pair_clusters <= 0) c->pair_clusters = prop.multiProcessorCount / 2;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   auto fail = [&](gqa_status st) {
     attn_destroy(c);

@@ -20,6 +20,9 @@ size_t decode_smem();
 // One-time per-process opt-in to large dynamic shared memory on the current device.
 cudaError_t configure_kernels();
 
+// Number of 2-CTA clusters of the pair GEMM that can be resident at once (0 on error).
+int gemm_pair_max_clusters();
+
 cudaError_t launch_gemm_qkv_rope(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                                  int grid, cudaStream_t s);
 cudaError_t launch_gemm_store_f32(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
