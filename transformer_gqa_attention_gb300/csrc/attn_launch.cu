@@ -22,14 +22,12 @@ cudaError_t configure_kernels() {
 
 cudaError_t launch_flash_prefill(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                  const FlashParams& p, dim3 grid, cudaStream_t s) {
-  flash_prefill_kernel<<<grid, 384, FlashSmem::kBytes, s>>>(q, k, v, p);
-  return cudaGetLastError();
+  return launch_pdl(flash_prefill_kernel, grid, dim3(384), FlashSmem::kBytes, s, 0, q, k, v, p);
 }
 
 cudaError_t launch_decode_attn(const CUtensorMap& k, const CUtensorMap& v, const DecodeParams& p,
                                dim3 grid, cudaStream_t s) {
-  decode_attn_kernel<<<grid, 160, DecodeSmem::kBytes, s>>>(k, v, p);
-  return cudaGetLastError();
+  return launch_pdl(decode_attn_kernel, grid, dim3(160), DecodeSmem::kBytes, s, 0, k, v, p);
 }
 
 cudaError_t launch_decode_combine(const DecodeParams& p, int B, cudaStream_t s) {

@@ -10,8 +10,9 @@
 //               16-row A operand); online softmax in fp32 with quad-shuffle row max/sum
 //   warp 4      producer: 64-key K and V tiles by TMA (128-byte swizzle), 3 stages
 //
-// Each CTA writes an unnormalised partial (O, running max m, running sum l) per head;
-// decode_combine_kernel merges the splits (log-sum-exp) and writes H bf16 [B, 4096].
+// Each CTA writes an unnormalised partial (O, running max m, running sum l) per head; the
+// last split of each (b, g) to finish merges the splits (log-sum-exp) and writes H bf16
+// [B, 4096] (or, without arrival counters, decode_combine_kernel does the merge).
 #pragma once
 
 #include "params.h"
@@ -33,6 +34,34 @@ struct DecodeSmem {
 // 64-key x 128-d tile stored as two 128-byte-swizzled 64-d halves.
 __device__ __forceinline__ uint32_t dec_chunk_off(int key, int cd) {
   return (cd >> 3) * DecodeSmem::kHalf + key * 128 + (((cd & 7) ^ (key & 7)) << 4);
+}
+
+// Merge the key splits of (b, g): H[b, h] = sum_s e^{m_s - M} O_s / sum_s e^{m_s - M} l_s.
+// 128 threads: thread -> (head 0..3, 4 consecutive d).  Partials are read from L2.
+__device__ __forceinline__ void decode_merge_splits(const DecodeParams& p, int b, int g, int tid) {
+  const int hh = tid >> 5;
+  const int d0 = (tid & 31) * 4;
+  const size_t unit0 = (static_cast<size_t>(b) * 8 + g) * p.n_splits;
+  float M = -INFINITY;
+  for (int s = 0; s < p.n_splits; ++s) M = fmaxf(M, __ldcg(p.part_ml + ((unit0 + s) * 4 + hh) * 2));
+  const float Mu = (M == -INFINITY) ? 0.f : M;
+  float Ls = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < p.n_splits; ++s) {
+    const size_t u = (unit0 + s) * 4 + hh;
+    const float f = fast_exp2(__ldcg(p.part_ml + u * 2) - Mu);
+    Ls += f * __ldcg(p.part_ml + u * 2 + 1);
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + u * 128 + d0));
+    acc[0] += f * v.x;
+    acc[1] += f * v.y;
+    acc[2] += f * v.z;
+    acc[3] += f * v.w;
+  }
+  const float inv = 1.f / Ls;
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.H) + static_cast<size_t>(b) * 4096 + (g * 4 + hh) * 128 + d0;
+  uint2 w;
+  w.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  w.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+  *reinterpret_cast<uint2*>(dst) = w;
 }
 
 __global__ void __launch_bounds__(160)
@@ -65,6 +94,10 @@ __global__ void __launch_bounds__(160)
     fence_mbar_init();
   }
   __syncthreads();
+  griddep_launch_dependents();
+  // q and the new cache entries come from the projection kernel; partials and counters
+  // may still be in use by an earlier kernel until it has finished
+  griddep_wait();
 
   if (warp == 4) {
     // ------------------------------------------------------------------ producer
@@ -196,8 +229,8 @@ __global__ void __launch_bounds__(160)
         red_ml[(warp * 4 + hh) * 2 + 1] = l_run;
       }
     }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (ok && !*abort_flag) {
+    // one decision for all 128 consumer threads (the merge below uses named barriers)
+    if (bar1_and_128(ok && !*abort_flag)) {
       const int tid = threadIdx.x;  // 0..127 -> (head, 4 d values)
       const int hh = tid >> 5;
       const int d0 = (tid & 31) * 4;
@@ -222,38 +255,27 @@ __global__ void __launch_bounds__(160)
         p.part_ml[(unit * 4 + hh) * 2 + 0] = M;
         p.part_ml[(unit * 4 + hh) * 2 + 1] = Ls;
       }
+      if (p.counters) {
+        // the last split of (b, g) to publish its partial merges all of them
+        volatile int* last_flag = abort_flag + 1;
+        __threadfence();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (tid == 0) *last_flag = (atomicAdd(&p.counters[b * 8 + g], 1) == p.n_splits - 1);
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (*last_flag) {
+          __threadfence();
+          decode_merge_splits(p, b, g, tid);
+          if (tid == 0) p.counters[b * 8 + g] = 0;  // ready for the next call
+        }
+      }
     }
   }
 }
 
-// Merge the key splits of each (b, g): H[b, h] = sum_s e^{m_s - M} O_s / sum_s e^{m_s - M} l_s.
-// grid (8, B), 128 threads: thread -> (head 0..3, 4 consecutive d).
+// Separate merge kernel (used when the decode kernel runs without arrival counters).
+// grid (8, B), 128 threads.
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
-  const int g = blockIdx.x;
-  const int b = blockIdx.y;
-  const int hh = threadIdx.x >> 5;
-  const int d0 = (threadIdx.x & 31) * 4;
-  const size_t unit0 = (static_cast<size_t>(b) * 8 + g) * p.n_splits;
-  float M = -INFINITY;
-  for (int s = 0; s < p.n_splits; ++s) M = fmaxf(M, p.part_ml[((unit0 + s) * 4 + hh) * 2]);
-  const float Mu = (M == -INFINITY) ? 0.f : M;
-  float Ls = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int s = 0; s < p.n_splits; ++s) {
-    const size_t u = (unit0 + s) * 4 + hh;
-    const float f = fast_exp2(p.part_ml[u * 2] - Mu);
-    Ls += f * p.part_ml[u * 2 + 1];
-    const float4 v = *reinterpret_cast<const float4*>(p.part_o + u * 128 + d0);
-    acc[0] += f * v.x;
-    acc[1] += f * v.y;
-    acc[2] += f * v.z;
-    acc[3] += f * v.w;
-  }
-  const float inv = 1.f / Ls;
-  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.H) + static_cast<size_t>(b) * 4096 + (g * 4 + hh) * 128 + d0;
-  uint2 w;
-  w.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-  w.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-  *reinterpret_cast<uint2*>(dst) = w;
+  decode_merge_splits(p, blockIdx.y, blockIdx.x, threadIdx.x);
 }
 
 }  // namespace gqa

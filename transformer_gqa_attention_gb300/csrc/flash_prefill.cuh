@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      griddep_wait();  // Q_r, K_r, V come from the projection kernel
       mbar_arrive_expect_tx(q_full, 2 * L::kTile);
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -211,26 +213,29 @@ __global__ void __launch_bounds__(384, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[slot], j & 1, abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(t_s + c * 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
-      }
+      // All four TMEM loads in flight before the single wait.
+      uint32_t sv[128];
+      tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[64]));
+      tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&sv[96]));
+      tmem_ld_wait();
       const int key0 = j * 128;
       const bool needs_mask = (key0 + 127 >= kv_len) || (p.causal && key0 + 127 > p.start_pos + q0);
       if (needs_mask) {
         const int lim = p.causal ? min(kv_len - 1, qpos) : kv_len - 1;
 #pragma unroll
         for (int i = 0; i < 128; ++i)
-          if (key0 + i > lim) s[i] = -INFINITY;
+          if (key0 + i > lim) sv[i] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
+      // Row max as 8 independent chains (max is exact in any order).
+      float m8[8];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) mx = fmaxf(mx, s[i]);
+      for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(sv[i]);
+#pragma unroll
+      for (int i = 8; i < 128; ++i) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(sv[i]));
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       const float m_tile = mx * p.scale_log2;
       // Per-row lazy rescale decision (rows never influence each other's bits).
       float alpha = 1.f;
@@ -244,20 +249,22 @@ __global__ void __launch_bounds__(384, 1)
         m_used = m_tile;
       }
       const float mu = (m_used == -INFINITY) ? 0.f : m_used;
-      // P = exp2(s * scale_log2 - m_used), bf16, written over S_i in TMEM.
-      float lsum = 0.f;
+      // P = exp2(s * scale_log2 - m_used), bf16, written over S_i in TMEM; the row sum
+      // accumulates in 8 independent partial sums.
+      float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = fast_exp2(fmaf(s[c * 32 + 2 * e], p.scale_log2, -mu));
-          const float p1 = fast_exp2(fmaf(s[c * 32 + 2 * e + 1], p.scale_log2, -mu));
-          lsum += p0 + p1;
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c * 32 + 2 * e]), p.scale_log2, -mu));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c * 32 + 2 * e + 1]), p.scale_log2, -mu));
+          l8[e & 7] += p0 + p1;
           w[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(t_s + c * 16, w);
       }
+      const float lsum = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
       l_sum += lsum;
       // O_i holds the sum through key tile j-1 (PV_i(j-1) completed before S_i(j)).
       if (__any_sync(0xffffffffu, grow)) {

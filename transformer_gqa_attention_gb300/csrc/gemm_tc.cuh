@@ -1,17 +1,19 @@
-// gemm_tc.cuh — persistent, warp-specialised tcgen05 GEMM, D[M,N] = A[M,K] * B[N,K]^T,
-// both operands K-major bf16 (the [out, in] weight storage of the quoted F.linear
-// layers), fp32 accumulation in TMEM.
+// gemm_tc.cuh — tcgen05 GEMMs of the block's projections, D = A * B^T with both operands
+// K-major bf16 (the [out, in] weight storage of the quoted F.linear layers) and fp32
+// accumulation in TMEM.  Two kernels:
 //
-//   warp 0      TMA producer: 128x64 A box + BNx64 B box per stage, 128-byte swizzle,
-//               one stage ring shared by all the CTA's work units
-//   warp 1      TMEM owner + single-thread UMMA issuer (128 x BN x 16 per instruction)
-//               into one of two TMEM accumulators (2 x BN columns)
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows, fused output transform;
-//               while it drains one accumulator the issuer fills the other, so the
-//               epilogue of unit i runs under the main loop of unit i+1
+//   gemm_tc_pair_kernel (many tokens) — persistent CTA pairs (cta_group::2), 256x256
+//     output tiles, double-buffered TMEM accumulators so the epilogue of one tile runs
+//     under the main loop of the next.  Warp roles per CTA: warp 0 TMA producer, warp 1
+//     TMEM owner (+ the single UMMA-issuing thread in CTA 0 of the pair), warps 2..5
+//     epilogue.  Tiles are numbered with the n tile fastest so the pairs resident at one
+//     time share A row bands through L2.
+//   gemm_splitk_cluster_kernel (few tokens) — swap-AB split-K over a thread-block cluster
+//     with the reduction done through distributed shared memory.
 //
-// Work units (m tile, n tile, k split) are numbered with the n tile fastest, so the CTAs
-// resident at one time share A row bands through L2; CTA c takes units c, c+G, c+2G, ...
+// Operands are read through 3-D tensor maps (64 columns, rows, 64-column k block), box
+// 64 x {64,128} x 1, so the same kernels read row-major activations (k-block stride 128 B)
+// and the k-block-major weight copies the context keeps (each box one contiguous 16 KB).
 //
 // Epilogues:
 //   kQkvRope  — the fused Q/K/V projection (steps 1-5 of "Llama 3.1 8B · Grouped-query
@@ -20,9 +22,7 @@
 //               R[t, j] in fp32, then Q is stored to the Q_r buffer [B*T,4096] and K_r, V
 //               straight into the caches [B,S_max,8,128] at position start_pos + t.
 //   kStoreF32 — Delta = H W_O^T (step 14) stored fp32 row-major.
-//   kPartialT — skinny (swap-AB) split-K: A holds weight rows, B the few token rows;
-//               each split stores its fp32 partial slab [token][feature] for a
-//               separate reduction kernel.
+//   kSplitKQkv / kSplitKOut — the same two epilogues for the few-token kernel.
 #pragma once
 
 #include "params.h"
@@ -37,23 +37,7 @@ struct GemmSmem {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kBarOffset = STAGES * kStageBytes;
   static constexpr int kBytes = kBarOffset + 256 + 1024;  // + barriers + alignment slack
-  static constexpr int kTmemCols = 2 * BN;                // two accumulators
 };
-
-struct GemmUnit {
-  int m0, n0, split, kb0, nkb;
-};
-
-__device__ __forceinline__ GemmUnit gemm_unit(const GemmParams& p, int u, int BN) {
-  GemmUnit w;
-  w.split = u % p.splits;
-  const int tile = u / p.splits;
-  w.n0 = (tile % p.n_tiles) * BN;
-  w.m0 = (tile / p.n_tiles) * 128;
-  w.kb0 = w.split * p.kb_per_split;
-  w.nkb = (w.split == p.splits - 1) ? (p.num_kb - w.kb0) : p.kb_per_split;
-  return w;
-}
 
 // Transform and store 32 accumulator columns (col0 .. col0+31) of output row m.
 template <int EPI>
@@ -97,154 +81,6 @@ __device__ __forceinline__ void gemm_epilogue_chunk(const GemmParams& p, int m, 
     for (int i = 0; i < 8; ++i)
       d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
                           __uint_as_float(v[4 * i + 3]));
-  } else {  // kPartialT: slab [split][token][feature]; a warp stores 32 consecutive features
-    float* base = static_cast<float*>(p.out0) + static_cast<size_t>(split) * p.slab +
-                  static_cast<size_t>(col0) * p.ldo + m;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) base[static_cast<size_t>(i) * p.ldo] = __uint_as_float(v[i]);
-  }
-}
-
-template <int BN, int STAGES, int EPI>
-__global__ void __launch_bounds__(192, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p) {
-  using L = GemmSmem<BN, STAGES>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * L::kABytes;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
-  uint64_t* empty_bar = full_bar + STAGES;
-  uint64_t* acc_full = empty_bar + STAGES;  // [2]
-  uint64_t* acc_empty = acc_full + 2;       // [2]
-  uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int total_units = p.m_tiles * p.n_tiles * p.splits;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 128);
-    }
-    mbar_init(drain, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_holder, L::kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_holder;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ TMA producer
-      tma_prefetch_desc(&tmA);
-      tma_prefetch_desc(&tmB);
-      int it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const GemmUnit w = gemm_unit(p, u, BN);
-        for (int i = 0; i < w.nkb; ++i, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full_bar[s], L::kStageBytes);
-          const int kc = (w.kb0 + i) * 64;
-          tma_load_2d(sA + s * L::kABytes, &tmA, &full_bar[s], kc, w.m0);
-          tma_load_2d(sB + s * L::kBBytes, &tmB, &full_bar[s], kc, w.n0);
-        }
-      }
-      if (*abort_flag) {  // let copies still in flight land before the CTA leaves
-        for (int i = (it > STAGES ? it - STAGES : 0); i < it; ++i)
-          mbar_wait_drain(&full_bar[i % STAGES], (i / STAGES) & 1);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ UMMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(128, BN, 0, 0);
-      const uint32_t a_base = smem_u32(sA);
-      const uint32_t b_base = smem_u32(sB);
-      int it = 0, lt = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++lt) {
-        const GemmUnit w = gemm_unit(p, u, BN);
-        const int ab = lt & 1;
-        if (!mbar_wait(&acc_empty[ab], ((lt >> 1) & 1) ^ 1u, abort_flag, p.status)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + ab * BN;
-        for (int i = 0; i < w.nkb; ++i, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(&full_bar[s], ph, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t da = sdesc_sw128(a_base + s * L::kABytes + k * 32, 0, 1024);
-            const uint64_t db = sdesc_sw128(b_base + s * L::kBBytes + k * 32, 0, 1024);
-            umma_ss(d_tmem, da, db, idesc, (i | k) != 0);
-          }
-          umma_commit(&empty_bar[s]);
-        }
-        if (ok) umma_commit(&acc_full[ab]);
-      }
-      if (*abort_flag) {  // let issued UMMAs finish before TMEM is released
-        umma_commit(drain);
-        mbar_wait_drain(drain, 0);
-      }
-    }
-  } else {
-    // -------------------------------------------------------------- epilogue
-    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-    const int row = quarter * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    int lt = 0;
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++lt) {
-      const GemmUnit w = gemm_unit(p, u, BN);
-      const int ab = lt & 1;
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[ab], (lt >> 1) & 1, abort_flag, p.status));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t t_row = tmem_base + lane_off + ab * BN;
-      const int m = w.m0 + row;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(t_row + c * 32, v);
-        tmem_ld_wait();
-        gemm_epilogue_chunk<EPI>(p, m, w.n0 + c * 32, w.split, v);
-      }
-      tc_fence_before();
-      mbar_arrive(&acc_empty[ab]);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, L::kTmemCols);
   }
 }
 
@@ -317,6 +153,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   cluster_sync();  // peer barriers initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -325,20 +162,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       tma_prefetch_desc(&tmB);
       int it = 0;
       bool ok = true;
+      // B is the context's weight copy (never written after creation): its first stages are
+      // fetched before waiting for the previous kernel; A (activations) only after.
+      const int n_pre = (pair < total_units) ? min(STAGES, p.num_kb) : 0;
+      if (n_pre > 0) {
+        const int n0 = (pair % p.n_tiles) * 256 + 128 * rank;
+        for (int i = 0; i < n_pre; ++i) {
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[i], 2 * L::kStageBytes);
+          tma_load_3d_pair(sB + i * L::kBBytes, &tmB, mapa_shared(smem_u32(&full_bar[i]), 0), 0, n0, i);
+        }
+      }
+      griddep_wait();
       for (int u = pair; ok && u < total_units; u += n_pairs) {
         const int m0 = (u / p.n_tiles) * 256 + 128 * rank;
         const int n0 = (u % p.n_tiles) * 256 + 128 * rank;
         for (int i = 0; i < p.num_kb; ++i, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
+          const uint32_t bar0 = mapa_shared(smem_u32(&full_bar[s]), 0);
+          if (it < n_pre) {  // B already requested above
+            tma_load_3d_pair(sA + s * L::kABytes, &tmA, bar0, 0, m0, i);
+            continue;
+          }
           if (!mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * L::kStageBytes);
-          const uint32_t bar0 = mapa_shared(smem_u32(&full_bar[s]), 0);
-          tma_load_2d_pair(sA + s * L::kABytes, &tmA, bar0, i * 64, m0);
-          tma_load_2d_pair(sB + s * L::kBBytes, &tmB, bar0, i * 64, n0);
+          tma_load_3d_pair(sA + s * L::kABytes, &tmA, bar0, 0, m0, i);
+          tma_load_3d_pair(sB + s * L::kBBytes, &tmB, bar0, 0, n0, i);
         }
       }
       if (*abort_flag && rank == 0) {  // CTA 0's barriers count both CTAs' bytes
@@ -415,6 +267,191 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, L::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Few-token projections (swap-AB: A = 128 weight rows = output features, B = the <= 64
+// token rows), split along K over the CTAs of one thread-block cluster (cluster rank =
+// split).  Each CTA accumulates its K range in TMEM, parks the fp32 partial tile
+// [64 tokens][128 features] in its own shared memory, and after one cluster barrier reduces
+// its share of the tokens by reading the partial tiles of all CTAs of the cluster
+// (distributed shared memory), then applies the final epilogue:
+//   kSplitKQkv — RoPE of Q and K pairs (adjacent lanes hold a pair), Q_r and the cache
+//                entries stored bf16 (steps 1-5);
+//   kSplitKOut — Delta stored fp32 (step 14).
+template <int EPI, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    gemm_splitk_cluster_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                               const GemmParams p) {
+  constexpr int BN = 64;
+  using L = GemmSmem<BN, STAGES>;
+  static_assert(STAGES * L::kStageBytes >= 64 * 128 * 4, "partial tile must fit in the stage buffers");
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * L::kABytes;
+  float* red = reinterpret_cast<float*>(smem);  // [64][128] partial tile, after the main loop
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* acc_full = empty_bar + STAGES;
+  uint64_t* drain = acc_full + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int split = static_cast<int>(cluster_ctarank());
+  const int m0 = (blockIdx.x / p.splits) * 128;
+  const int kb0 = split * p.num_kb / p.splits;
+  const int nkb = (split + 1) * p.num_kb / p.splits - kb0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, BN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  griddep_launch_dependents();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      // A is the context's weight copy (never written after creation): its first stages are
+      // fetched before waiting for the previous kernel; B (activations) only after.
+      const int n_pre = min(STAGES, nkb);
+      for (int i = 0; i < n_pre; ++i) {
+        mbar_arrive_expect_tx(&full_bar[i], L::kStageBytes);
+        tma_load_3d(sA + i * L::kABytes, &tmA, &full_bar[i], 0, m0, kb0 + i);
+      }
+      griddep_wait();
+      int issued = 0;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % STAGES;
+        if (i >= n_pre) {
+          if (!mbar_wait(&empty_bar[s], ((i / STAGES) & 1) ^ 1u, abort_flag, p.status)) break;
+          mbar_arrive_expect_tx(&full_bar[s], L::kStageBytes);
+          tma_load_3d(sA + s * L::kABytes, &tmA, &full_bar[s], 0, m0, kb0 + i);
+        }
+        tma_load_3d(sB + s * L::kBBytes, &tmB, &full_bar[s], 0, 0, kb0 + i);
+        ++issued;
+      }
+      if (*abort_flag) {
+        for (int i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
+          mbar_wait_drain(&full_bar[i % STAGES], (i / STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, BN, 0, 0);
+      const uint32_t a_base = smem_u32(sA);
+      const uint32_t b_base = smem_u32(sB);
+      bool ok = true;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % STAGES;
+        if (!(ok = mbar_wait(&full_bar[s], (i / STAGES) & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ss(tmem_base, sdesc_sw128(a_base + s * L::kABytes + k * 32, 0, 1024),
+                  sdesc_sw128(b_base + s * L::kBBytes + k * 32, 0, 1024), idesc, (i | k) != 0);
+        umma_commit(&empty_bar[s]);
+      }
+      umma_commit(ok ? acc_full : drain);
+      if (!ok) mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // accumulator rows (features) -> this CTA's partial tile in shared memory
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    if (bar1_and_128(mbar_wait(acc_full, 0, abort_flag, p.status))) {
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) red[(c * 32 + i) * 128 + row] = __uint_as_float(v[i]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // every split's partial tile is in its CTA's shared memory
+
+  if (warp >= 2 && !*abort_flag) {
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int m = m0 + row;
+    const int t_lo = split * p.N / p.splits;
+    const int t_hi = (split + 1) * p.N / p.splits;
+    const uint32_t red_addr = smem_u32(red);
+    // 4 tokens per pass, all splits' loads issued before the sums are used
+    for (int tok0 = t_lo; tok0 < t_hi; tok0 += 4) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if (r < p.splits) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int tok = min(tok0 + q, t_hi - 1);
+            acc[q] += ld_shared_cluster_f32(mapa_shared(red_addr + (tok * 128 + row) * 4, r));
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int tok = tok0 + q;
+        if (tok >= t_hi) break;
+        if constexpr (EPI == kSplitKOut) {
+          static_cast<float*>(p.fin0)[static_cast<size_t>(tok) * 4096 + m] = acc[q];
+        } else {
+          // rotation pairs (2j, 2j+1) are held by adjacent lanes
+          const float partner = __shfl_xor_sync(0xffffffffu, acc[q], 1);
+          const int b = tok / p.T;
+          const int t = tok - b * p.T;
+          float outv = acc[q];
+          if (m < 5120) {
+            const float2 cs =
+                __ldg(reinterpret_cast<const float2*>(p.R) + static_cast<size_t>(t) * 64 + ((m & 127) >> 1));
+            outv = (lane & 1) ? (cs.y * partner + cs.x * acc[q]) : (cs.x * acc[q] - cs.y * partner);
+          }
+          const __nv_bfloat16 o = __float2bfloat16_rn(outv);
+          if (m < 4096) {
+            static_cast<__nv_bfloat16*>(p.fin0)[static_cast<size_t>(tok) * 4096 + m] = o;
+          } else {
+            const bool is_v = m >= 5120;
+            const size_t crow = static_cast<size_t>(b) * p.S_max + p.start_pos + t;
+            static_cast<__nv_bfloat16*>(is_v ? p.fin2 : p.fin1)[crow * 1024 + (m - (is_v ? 5120 : 4096))] = o;
+          }
+        }
+      }
+    }
+  }
+
+  // no CTA leaves while its partial tile may still be read (the reads have completed once
+  // their values were summed, so no release ordering is needed)
+  cluster_sync_relaxed();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, BN);
   }
 }
 

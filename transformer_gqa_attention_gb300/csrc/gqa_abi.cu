@@ -22,9 +22,11 @@ struct gqa_ctx {
   int device = -1;
   int num_sms = 0;
   int pair_clusters = 0;  // co-resident 2-CTA clusters of the pair GEMM
-  __nv_bfloat16* w_qkv = nullptr;  // [6144, 4096]: W_Q rows 0..4095, W_K 4096..5119, W_V 5120..6143
-  __nv_bfloat16* w_o = nullptr;    // [4096, 4096]
+  // weights, k-block-major: W_t[kb][row][64] for kb = 0..63
+  __nv_bfloat16* w_qkv = nullptr;  // 6144 rows: W_Q rows 0..4095, W_K 4096..5119, W_V 5120..6143
+  __nv_bfloat16* w_o = nullptr;    // 4096 rows
   int* status = nullptr;           // device status word (kDevErr* bits)
+  int* counters = nullptr;         // arrival counters of the decode split merge (kCounterInts)
   uint8_t* ws = nullptr;           // workspace
   size_t ws_bytes = 0;
   const void* last_q = nullptr;
@@ -57,6 +59,8 @@ constexpr long long kMaxTokens = 262144;
 constexpr long long kMaxSMax = 1048576;
 constexpr int kSkinnyMaxTokens = 64;     // at or below: swap-AB split-K projections
 constexpr int kDecodeMaxBatch = 1024;
+// Arrival counters of the decode split merge, one per (sequence, kv group).
+constexpr int kCounterInts = kDecodeMaxBatch * 8;
 
 // ------------------------------------------------------------------ tensor maps
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -96,12 +100,35 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Row-major [rows, 4096] bf16 matrix, box 64 (K) x box_rows.
+// GEMM operands are addressed as (column c < 64, row r, k block kb) with box 64 x box_rows x 1.
+// Row-major [rows, 4096] activation: element (c, r, kb) at r*8192 + kb*128 + 2c bytes.
 bool map_rows_k4096(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
-  const uint64_t dims[2] = {4096, rows};
-  const uint64_t strides[1] = {4096 * 2};
-  const uint32_t box[2] = {64, box_rows};
-  return make_map(m, base, 2, dims, strides, box);
+  const uint64_t dims[3] = {64, rows, 64};
+  const uint64_t strides[2] = {4096 * 2, 64 * 2};
+  const uint32_t box[3] = {64, box_rows, 1};
+  return make_map(m, base, 3, dims, strides, box);
+}
+
+// k-block-major weight copy W_t[kb][row][64]: element (c, r, kb) at (kb*rows + r)*128 + 2c
+// bytes, so one box of consecutive rows is one contiguous read.
+bool map_weight_tiled(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  const uint64_t dims[3] = {64, rows, 64};
+  const uint64_t strides[2] = {64 * 2, rows * 64 * 2};
+  const uint32_t box[3] = {64, box_rows, 1};
+  return make_map(m, base, 3, dims, strides, box);
+}
+
+// Copy a row-major [rows, 4096] bf16 weight into rows row0.. of a k-block-major copy with
+// total_rows rows (64 strided 2-D copies, at context creation only).
+cudaError_t copy_weight_tiled(void* dst, const void* src, size_t rows, size_t row0, size_t total_rows,
+                              cudaStream_t s) {
+  for (size_t kb = 0; kb < 64; ++kb) {
+    uint8_t* d = static_cast<uint8_t*>(dst) + (kb * total_rows + row0) * 128;
+    const uint8_t* from = static_cast<const uint8_t*>(src) + kb * 128;
+    cudaError_t e = cudaMemcpy2DAsync(d, 128, from, 8192, 128, rows, cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // KV cache [B, S_max, 8, 128] bf16 seen as (d, g, s < kv_len, b); box 64 d x key_rows.
@@ -116,7 +143,7 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // ------------------------------------------------------------------ workspace
 struct WsLayout {
-  size_t q_off, h_off, part_off, dec_o_off, dec_ml_off, total;
+  size_t q_off, h_off, dec_o_off, dec_ml_off, total;
 };
 
 struct SkinnyPlan {
@@ -127,9 +154,11 @@ SkinnyPlan skinny_plan(int n_tok, int num_sms) {
   SkinnyPlan s;
   s.n_tiles = (n_tok + 63) / 64;
   s.tok_pad = s.n_tiles * 64;
-  // about two CTAs per SM; each split keeps at least 4 k-blocks of 64
-  s.splits_qkv = std::max(1, std::min(16, (2 * num_sms) / (48 * s.n_tiles)));
-  s.splits_o = std::max(1, std::min(16, (2 * num_sms) / (32 * s.n_tiles)));
+  // k splits = cluster size, one CTA per SM; all clusters must be co-resident (GB300
+  // holds 76 two-CTA or 36 four-CTA clusters of this kernel): 48 x 2 and 32 x 4 CTAs
+  (void)num_sms;
+  s.splits_qkv = 2;
+  s.splits_o = 4;
   return s;
 }
 
@@ -157,12 +186,6 @@ WsLayout ws_layout(long long n_tok, const SkinnyPlan* sk, const DecodePlan* dp, 
   off = round_up(off + static_cast<size_t>(n_tok) * 4096 * 2, 256);
   w.h_off = off;
   off = round_up(off + static_cast<size_t>(n_tok) * 4096 * 2, 256);
-  w.part_off = off;
-  if (sk) {
-    const size_t a = static_cast<size_t>(sk->splits_qkv) * sk->tok_pad * 6144;
-    const size_t b = static_cast<size_t>(sk->splits_o) * sk->tok_pad * 4096;
-    off = round_up(off + std::max(a, b) * 4, 256);
-  }
   w.dec_o_off = off;
   w.dec_ml_off = off;
   if (dp) {
@@ -241,7 +264,7 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
   p.num_kb = 64;
   CUtensorMap ta, tb;
   if (sk) {
-    if (!map_rows_k4096(&ta, c->w_qkv, 6144, 128) || !map_rows_k4096(&tb, x, n_tok, 64))
+    if (!map_weight_tiled(&ta, c->w_qkv, 6144, 128) || !map_rows_k4096(&tb, x, n_tok, 64))
       return cuda_fail(cudaErrorInvalidValue);
     p.M = 6144;
     p.N = n_tok;
@@ -249,27 +272,15 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
     p.kb_per_split = 64 / p.splits;
     p.n_tiles = sk->n_tiles;
     p.m_tiles = 48;
-    p.out0 = c->ws + w.part_off;
-    p.ldo = 6144;
-    p.slab = static_cast<long long>(sk->tok_pad) * 6144;
+    p.fin0 = q_out;
+    p.fin1 = ck;
+    p.fin2 = cv;
+    p.R = R;
     const int grid = std::min(p.m_tiles * p.n_tiles * p.splits, 2 * c->num_sms);
-    { ProfScope ps(c, GQA_KERNEL_QKV_SPLITK, s); GQA_CUDA(launch_gemm_partial(ta, tb, p, grid, s)); }
-    QkvFinalizeParams f{};
-    f.part = reinterpret_cast<const float*>(c->ws + w.part_off);
-    f.slab = p.slab;
-    f.splits = p.splits;
-    f.n_tok = n_tok;
-    f.T = T;
-    f.S_max = S_max;
-    f.start_pos = start_pos;
-    f.R = R;
-    f.q = q_out;
-    f.cache_k = ck;
-    f.cache_v = cv;
-    { ProfScope ps(c, GQA_KERNEL_QKV_FINALIZE, s); GQA_CUDA(launch_qkv_finalize(f, s)); }
+    { ProfScope ps(c, GQA_KERNEL_QKV_SPLITK, s); GQA_CUDA(launch_gemm_splitk_qkv(ta, tb, p, grid, s)); }
   } else {
     // CTA pairs, 256x256 tiles: each CTA loads 128-row boxes of x and of W_QKV
-    if (!map_rows_k4096(&ta, x, n_tok, 128) || !map_rows_k4096(&tb, c->w_qkv, 6144, 128))
+    if (!map_rows_k4096(&ta, x, n_tok, 128) || !map_weight_tiled(&tb, c->w_qkv, 6144, 128))
       return cuda_fail(cudaErrorInvalidValue);
     p.M = n_tok;
     p.N = 6144;
@@ -295,7 +306,7 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
   p.num_kb = 64;
   CUtensorMap ta, tb;
   if (sk) {
-    if (!map_rows_k4096(&ta, c->w_o, 4096, 128) || !map_rows_k4096(&tb, h, n_tok, 64))
+    if (!map_weight_tiled(&ta, c->w_o, 4096, 128) || !map_rows_k4096(&tb, h, n_tok, 64))
       return cuda_fail(cudaErrorInvalidValue);
     p.M = 4096;
     p.N = n_tok;
@@ -303,20 +314,11 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
     p.kb_per_split = 64 / p.splits;
     p.n_tiles = sk->n_tiles;
     p.m_tiles = 32;
-    p.out0 = c->ws + w.part_off;
-    p.ldo = 4096;
-    p.slab = static_cast<long long>(sk->tok_pad) * 4096;
+    p.fin0 = delta;
     const int grid = std::min(p.m_tiles * p.n_tiles * p.splits, 2 * c->num_sms);
-    { ProfScope ps(c, GQA_KERNEL_OUT_SPLITK, s); GQA_CUDA(launch_gemm_partial(ta, tb, p, grid, s)); }
-    OutFinalizeParams f{};
-    f.part = reinterpret_cast<const float*>(c->ws + w.part_off);
-    f.slab = p.slab;
-    f.splits = p.splits;
-    f.n_tok = n_tok;
-    f.delta = delta;
-    { ProfScope ps(c, GQA_KERNEL_OUT_FINALIZE, s); GQA_CUDA(launch_out_finalize(f, s)); }
+    { ProfScope ps(c, GQA_KERNEL_OUT_SPLITK, s); GQA_CUDA(launch_gemm_splitk_out(ta, tb, p, grid, s)); }
   } else {
-    if (!map_rows_k4096(&ta, h, n_tok, 128) || !map_rows_k4096(&tb, c->w_o, 4096, 128))
+    if (!map_rows_k4096(&ta, h, n_tok, 128) || !map_weight_tiled(&tb, c->w_o, 4096, 128))
       return cuda_fail(cudaErrorInvalidValue);
     p.M = n_tok;
     p.N = 4096;
@@ -378,19 +380,18 @@ gqa_status attn_create(const void* wq, const void* wk, const void* wv, const voi
   };
   if (cudaMalloc(&c->w_qkv, size_t(6144) * 4096 * 2) != cudaSuccess ||
       cudaMalloc(&c->w_o, size_t(4096) * 4096 * 2) != cudaSuccess ||
-      cudaMalloc(&c->status, sizeof(int)) != cudaSuccess) {
+      cudaMalloc(&c->status, sizeof(int)) != cudaSuccess ||
+      cudaMalloc(&c->counters, kCounterInts * sizeof(int)) != cudaSuccess) {
     cudaGetLastError();
     return fail(GQA_ERR_OOM);
   }
-  const size_t wq_b = size_t(4096) * 4096 * 2, wkv_b = size_t(1024) * 4096 * 2;
   cudaError_t e = cudaMemsetAsync(c->status, 0, sizeof(int), s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(c->w_qkv, wq, wq_b, cudaMemcpyDeviceToDevice, s);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(c->w_qkv) + wq_b, wk, wkv_b, cudaMemcpyDeviceToDevice, s);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(c->w_qkv) + wq_b + wkv_b, wv, wkv_b,
-                        cudaMemcpyDeviceToDevice, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(c->w_o, wo, wq_b, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->counters, 0, kCounterInts * sizeof(int), s);
+  // k-block-major copies: W_Q rows 0..4095, W_K 4096..5119, W_V 5120..6143 of W_QKV; W_O
+  if (e == cudaSuccess) e = copy_weight_tiled(c->w_qkv, wq, 4096, 0, 6144, s);
+  if (e == cudaSuccess) e = copy_weight_tiled(c->w_qkv, wk, 1024, 4096, 6144, s);
+  if (e == cudaSuccess) e = copy_weight_tiled(c->w_qkv, wv, 1024, 5120, 6144, s);
+  if (e == cudaSuccess) e = copy_weight_tiled(c->w_o, wo, 4096, 0, 4096, s);
   if (e != cudaSuccess) return fail(cuda_fail(e));
   *out = c;
   return GQA_OK;
@@ -491,8 +492,8 @@ gqa_status attn_decode(gqa_ctx* c, const void* x, int B, int start_pos, const fl
   p.H = h;
   p.status = c->status;
   p.scale_log2 = kScaleLog2;
+  p.counters = c->counters;  // the last split of each (b, g) merges
   { ProfScope ps(c, GQA_KERNEL_DECODE_ATTN, s); GQA_CUDA(launch_decode_attn(tk, tv, p, dim3(dp.n_splits, 8, B), s)); }
-  { ProfScope ps(c, GQA_KERNEL_DECODE_COMBINE, s); GQA_CUDA(launch_decode_combine(p, B, s)); }
 
   // step 14
   return run_out(c, h, B, delta, w, sk, s);
@@ -505,6 +506,8 @@ gqa_status attn_sync_status(gqa_ctx* c, gqa_stream_t stream) {
   int v = 0;
   GQA_CUDA(cudaMemcpy(&v, c->status, sizeof(int), cudaMemcpyDeviceToHost));
   if (v != 0) {
+    // an aborted kernel may have left arrival counters mid-count
+    GQA_CUDA(cudaMemset(c->counters, 0, kCounterInts * sizeof(int)));
     GQA_CUDA(cudaMemset(c->status, 0, sizeof(int)));
     if (v & kDevErrTimeout) return GQA_ERR_TIMEOUT;
   }
@@ -555,6 +558,7 @@ void attn_destroy(gqa_ctx* c) {
   if (c->w_qkv) cudaFree(c->w_qkv);
   if (c->w_o) cudaFree(c->w_o);
   if (c->status) cudaFree(c->status);
+  if (c->counters) cudaFree(c->counters);
   if (c->ws) cudaFree(c->ws);
   delete c;
 }

@@ -11,6 +11,34 @@
 
 namespace gqa {
 
+// Launch `kernel` with programmatic dependent launch (the kernel calls griddep_wait before
+// touching anything an earlier kernel may write) and, if cluster_x > 0, a runtime cluster
+// shape of cluster_x x 1 x 1.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster_x,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Dynamic shared memory each kernel needs (bytes).
 size_t gemm_wide_smem();    // 128x256 tiles (prefill)
 size_t gemm_skinny_smem();  // 128x64 tiles (few tokens, split-K)
@@ -27,27 +55,11 @@ cudaError_t launch_gemm_qkv_rope(const CUtensorMap& a, const CUtensorMap& b, con
                                  int grid, cudaStream_t s);
 cudaError_t launch_gemm_store_f32(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                                   int grid, cudaStream_t s);
-cudaError_t launch_gemm_partial(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                                int grid, cudaStream_t s);
-
-// Reduction of the skinny projection partials.
-struct QkvFinalizeParams {
-  const float* part;  // [splits][tokens_pad][6144]
-  long long slab;
-  int splits, n_tok, T, S_max, start_pos;
-  const float* R;     // [T,64,2]
-  void* q;            // [n_tok, 4096] bf16
-  void* cache_k;      // [B,S_max,8,128] bf16
-  void* cache_v;
-};
-struct OutFinalizeParams {
-  const float* part;  // [splits][tokens_pad][4096]
-  long long slab;
-  int splits, n_tok;
-  float* delta;       // [n_tok, 4096]
-};
-cudaError_t launch_qkv_finalize(const QkvFinalizeParams& p, cudaStream_t s);
-cudaError_t launch_out_finalize(const OutFinalizeParams& p, cudaStream_t s);
+// Few-token split-K projections with the reduction fused (last split of each tile).
+cudaError_t launch_gemm_splitk_qkv(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                                   int grid, cudaStream_t s);
+cudaError_t launch_gemm_splitk_out(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                                   int grid, cudaStream_t s);
 
 cudaError_t launch_flash_prefill(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                  const FlashParams& p, dim3 grid, cudaStream_t s);

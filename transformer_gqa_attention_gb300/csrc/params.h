@@ -13,23 +13,27 @@ constexpr int kDevErrTimeout = 1;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s while draining after an abort
 
-enum EpiMode : int { kQkvRope = 0, kStoreF32 = 1, kPartialT = 2 };
+// kQkvRope / kStoreF32: many-token epilogues.  kSplitKQkv / kSplitKOut: the same two
+// epilogues after the cluster-wide split-K reduction of the few-token kernel.
+enum EpiMode : int { kQkvRope = 0, kStoreF32 = 1, kSplitKQkv = 3, kSplitKOut = 4 };
 
 struct GemmParams {
   int M, N;          // rows of A, rows of B
   int num_kb;        // K / 64
-  int kb_per_split;  // k-blocks per split (last split takes the remainder)
-  int splits;
+  int kb_per_split;  // unused by the kernels (k ranges are split evenly)
+  int splits;        // few-token kernel: k splits = cluster size
   int n_tiles;       // ceil(N / BN)
   int m_tiles;       // ceil(M / 128)
   // epilogue operands
-  void* out0;        // kQkvRope: Q_r [M,4096] bf16 | kStoreF32: D fp32 | kPartialT: partial base
+  void* out0;        // kQkvRope: Q_r [M,4096] bf16 | kStoreF32: D fp32
   void* out1;        // kQkvRope: cache_k
   void* out2;        // kQkvRope: cache_v
-  const float* R;    // kQkvRope: [T,64,2]
+  const float* R;    // Q/K/V epilogues: [T,64,2]
   int T, S_max, start_pos;
-  int ldo;           // kStoreF32: row stride (floats) | kPartialT: features per token row
-  long long slab;    // kPartialT: elements per split slab
+  int ldo;           // kStoreF32: row stride (floats)
+  void* fin0;        // split-K final outputs: Q_r [N,4096] bf16 | Delta [N,4096] fp32
+  void* fin1;        // kSplitKQkv: cache_k
+  void* fin2;        // kSplitKQkv: cache_v
   int* status;
 };
 
@@ -49,6 +53,7 @@ struct DecodeParams {
   const void* q;  // [B, 4096] bf16 rotated queries
   float* part_o;           // [B, 8, n_splits, 4, 128]
   float* part_ml;          // [B, 8, n_splits, 4, 2]
+  int* counters;           // [B*8] arrival counters: the last split merges (null: separate merge kernel)
   void* H;        // [B, 4096] bf16 (combine output)
   int* status;
   float scale_log2;
