@@ -11,8 +11,10 @@
 //   warp 1      TMEM owner + UMMA issuer.  Per key tile j, for head slot i = 0, 1:
 //                 S_i = Q_i K_j^T (both operands K-major from shared memory) into TMEM,
 //                 O_i += P_i V_j with P_i read from TMEM (it overwrites S_i) and V an
-//                 MN-major shared-memory operand.  Issue order S_0(j+1) before PV_1(j) keeps
-//                 the tensor core busy while the other head's softmax runs.
+//                 MN-major shared-memory operand, issued in two halves (keys 0..63 as soon
+//                 as the softmax has released them, then 64..127).  Issue order S_0(j+1)
+//                 before PV_1(j) keeps the tensor core busy while the other head's softmax
+//                 runs.
 //   warps 4..7  softmax of head slot 0, warps 8..11 of head slot 1: one thread per query
 //               row (no shuffles); online softmax in fp32 in the log2 domain with the
 //               1/sqrt(128) scale folded into the exponent; P = exp2(...) rounded to bf16
@@ -55,10 +57,11 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* v_full = bars + 5;   // [2]
   uint64_t* v_empty = bars + 7;  // [2]
   uint64_t* s_full = bars + 9;   // [2] head slots
-  uint64_t* p_full = bars + 11;  // [2] head slots, 128 arrivals
-  uint64_t* o_full = bars + 13;  // [2] head slots
-  uint64_t* drain = bars + 15;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* p_lo = bars + 11;    // [2] head slots, 128 arrivals: P of keys 0..63 in TMEM
+  uint64_t* p_hi = bars + 13;    // [2] head slots, 128 arrivals: P of keys 64..127
+  uint64_t* o_full = bars + 15;  // [2] head slots
+  uint64_t* drain = bars + 17;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -75,7 +78,7 @@ __global__ void __launch_bounds__(384, 1)
   const int n_kv = (kv_hi + 127) / 128;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 16; ++i) mbar_init(&bars[i], (i == 11 || i == 12) ? 128u : 1u);
+    for (int i = 0; i < 18; ++i) mbar_init(&bars[i], (i >= 11 && i <= 14) ? 128u : 1u);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -147,13 +150,14 @@ __global__ void __launch_bounds__(384, 1)
         }
         umma_commit(&s_full[i]);
       };
-      // O_i += P_i(j) V_j; P_i holds keys (2c, 2c+1) in column c of S_i's TMEM columns.
-      auto issue_pv = [&](int i, int j) {
+      // O_i += P_i(j) V_j for keys 16*kk0 .. 16*kk0+63 (kk0 = 0 or 4); P_i holds keys
+      // (2c, 2c+1) in column c of S_i's TMEM columns.
+      auto issue_pv_half = [&](int i, int j, int kk0) {
         const int st = j & 1;
         const uint32_t d_o = tmem_base + 256 + i * 128;
         const uint32_t a_p = tmem_base + i * 128;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = kk0; kk < kk0 + 4; ++kk) {
           // V: MN-major (d contiguous); 16 keys = two 8-row groups = 2048 B per step;
           // d 64..127 lives in the second half (LBO), 8-key groups 1024 B apart (SBO).
           umma_ts(d_o, a_p + kk * 8, sdesc_sw128(v_addr + st * L::kTile + kk * 2048, L::kHalf, 1024),
@@ -170,11 +174,14 @@ __global__ void __launch_bounds__(384, 1)
       }
       for (int j = 0; ok && j < n_kv; ++j) {
         const bool more = j + 1 < n_kv;
-        // head slot 0: PV_0(j), then S_0(j+1)
+        // head slot 0: PV_0(j) in two halves as P arrives, then S_0(j+1)
         if (!(ok = mbar_wait(&v_full[j & 1], (j >> 1) & 1, abort_flag, p.status))) break;
-        if (!(ok = mbar_wait(&p_full[0], j & 1, abort_flag, p.status))) break;
+        if (!(ok = mbar_wait(&p_lo[0], j & 1, abort_flag, p.status))) break;
         tc_fence_after();
-        issue_pv(0, j);
+        issue_pv_half(0, j, 0);
+        if (!(ok = mbar_wait(&p_hi[0], j & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        issue_pv_half(0, j, 4);
         if (!more) umma_commit(&o_full[0]);
         if (more) {
           if (!(ok = mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_flag, p.status))) break;
@@ -182,9 +189,12 @@ __global__ void __launch_bounds__(384, 1)
           issue_s(0, j + 1);
         }
         // head slot 1: PV_1(j), then S_1(j+1)
-        if (!(ok = mbar_wait(&p_full[1], j & 1, abort_flag, p.status))) break;
+        if (!(ok = mbar_wait(&p_lo[1], j & 1, abort_flag, p.status))) break;
         tc_fence_after();
-        issue_pv(1, j);
+        issue_pv_half(1, j, 0);
+        if (!(ok = mbar_wait(&p_hi[1], j & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        issue_pv_half(1, j, 4);
         umma_commit(&v_empty[j & 1]);
         if (!more) umma_commit(&o_full[1]);
         if (more) {
@@ -249,38 +259,42 @@ __global__ void __launch_bounds__(384, 1)
         m_used = m_tile;
       }
       const float mu = (m_used == -INFINITY) ? 0.f : m_used;
-      // P = exp2(s * scale_log2 - m_used), bf16, written over S_i in TMEM; the row sum
+      // P = exp2(s * scale_log2 - m_used), bf16, written over S_i in TMEM in two halves
+      // (keys 0..63, then 64..127), each released as soon as it is stored; the row sum
       // accumulates in 8 independent partial sums.
       float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t w[16];
+      for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c * 32 + 2 * e]), p.scale_log2, -mu));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c * 32 + 2 * e + 1]), p.scale_log2, -mu));
-          l8[e & 7] += p0 + p1;
-          w[e] = pack_bf16x2(p0, p1);
+        for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c * 32 + 2 * e]), p.scale_log2, -mu));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c * 32 + 2 * e + 1]), p.scale_log2, -mu));
+            l8[e & 7] += p0 + p1;
+            w[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(t_s + c * 16, w);
         }
-        tmem_st16(t_s + c * 16, w);
-      }
-      const float lsum = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-      l_sum += lsum;
-      // O_i holds the sum through key tile j-1 (PV_i(j-1) completed before S_i(j)).
-      if (__any_sync(0xffffffffu, grow)) {
+        if (hf == 0 && __any_sync(0xffffffffu, grow)) {
+          // O_i holds the sum through key tile j-1 (PV_i(j-1) completed before S_i(j)); it
+          // is rescaled before any part of P_i(j) is released to the tensor core.
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_ld32(t_o + c * 32, v);
+            tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(t_o + c * 32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tmem_st32(t_o + c * 32, v);
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(t_o + c * 32, v);
+          }
         }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(hf == 0 ? &p_lo[slot] : &p_hi[slot]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&p_full[slot]);
+      l_sum += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[slot], 0, abort_flag, p.status));
     if (ok) {
