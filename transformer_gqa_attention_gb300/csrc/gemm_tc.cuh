@@ -208,7 +208,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       bool ok = true;
       for (int u = pair; ok && u < total_units; u += n_pairs, ++lt) {
         const int ab = lt & 1;
-        if (!mbar_wait(&acc_empty[ab], ((lt >> 1) & 1) ^ 1u, abort_flag, p.status)) break;
+        if (!mbar_wait_cluster(&acc_empty[ab], ((lt >> 1) & 1) ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + ab * 256;
         for (int i = 0; i < p.num_kb; ++i, ++it) {

@@ -444,6 +444,7 @@ gqa_status attn_prefill(gqa_ctx* c, const void* x, int B, int T, const float* R,
   fp.H = h;
   fp.status = c->status;
   fp.scale_log2 = kScaleLog2;
+  // grid.x = (b, head pair), grid.y = query tiles
   { ProfScope ps(c, GQA_KERNEL_FLASH_PREFILL, s); GQA_CUDA(launch_flash_prefill(tq, tk, tv, fp, dim3(B * 16, fp.n_qtiles), s)); }
 
   return run_out(c, h, n_tok, delta, w, sk, s);
