@@ -196,6 +196,19 @@ gqa_status attn_decode_attention_noalloc(const void *q_r, const void *cache_k,
                                          const void *cache_v, int B, int kv_len, int S_max,
                                          void *h, gqa_stream_t stream);
 
+/*
+ * attn_debug_inject_timeout — test hook for the failure path (no counterpart on the pages).
+ * Arms a one-shot flag: on the next launch of kernel kind `kind` (GQA_KERNEL_QKV_GEMM,
+ * _QKV_SPLITK, _FLASH_PREFILL, _DECODE_ATTN, _OUT_GEMM or _OUT_SPLITK) made through this
+ * context, the first work unit's TMA producer issues no loads.  Its consumers' bounded
+ * waits then run out (about 2 s), the unit records GQA_ERR_TIMEOUT in the status word,
+ * releases its tensor memory and returns; kernels queued after it on the stream may time
+ * out too.  Nothing faults or hangs.  The outputs of that call are undefined; the next
+ * attn_sync_status returns GQA_ERR_TIMEOUT and resets the device-side state, after which
+ * the context is usable again.  Errors: GQA_ERR_INVALID_ARG (null context, other kind).
+ */
+gqa_status attn_debug_inject_timeout(gqa_ctx *ctx, int kind);
+
 /* attn_destroy — free everything the context owns (after synchronising the device).
  * NULL is ignored. */
 void attn_destroy(gqa_ctx *ctx);

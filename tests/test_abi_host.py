@@ -108,3 +108,8 @@ def test_null_context_calls(L):
     assert abi.raw_status("attn_sync_status", None, None) == 1
     assert abi.raw_status("attn_debug_buffers", None, None, None) == 1
     L.attn_destroy(None)  # ignored
+
+
+def test_timeout_hook_validation(L):
+    assert abi.raw_status("attn_debug_inject_timeout", None, 0) == 1
+    assert abi.raw_status("attn_debug_inject_timeout", vp(FAKE), 99) == 1

@@ -18,7 +18,8 @@ STATUS_NAMES = {0: "GQA_OK", 1: "GQA_ERR_INVALID_ARG", 2: "GQA_ERR_SHAPE", 3: "G
 
 # Every symbol include/gqa_attn.h declares.
 EXPORTED = ("attn_create", "attn_prefill", "attn_decode", "attn_sync_status", "attn_debug_buffers",
-            "attn_profile_begin", "attn_profile_end", "attn_decode_attention_noalloc",
+            "attn_profile_begin", "attn_profile_end", "attn_debug_inject_timeout",
+            "attn_decode_attention_noalloc",
             "attn_destroy", "attn_strerror", "attn_last_cuda_error")
 
 # Kernel kinds of attn_profile_end (GQA_KERNEL_* in include/gqa_attn.h).
@@ -62,6 +63,8 @@ def lib() -> ctypes.CDLL:
     L.attn_profile_begin.restype = i32
     L.attn_profile_end.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i32), vp]
     L.attn_profile_end.restype = i32
+    L.attn_debug_inject_timeout.argtypes = [vp, i32]
+    L.attn_debug_inject_timeout.restype = i32
     L.attn_decode_attention_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
     L.attn_decode_attention_noalloc.restype = i32
     L.attn_destroy.argtypes = [vp]
@@ -136,6 +139,13 @@ def attn_profile_end(ctx, stream=None):
     cnt = (ctypes.c_int * n)()
     _check("attn_profile_end", lib().attn_profile_end(ctx, ms, cnt, _stream(stream)))
     return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def attn_debug_inject_timeout(ctx, kind):
+    """Arm the one-shot failure-path test hook for the next launch of a kernel kind (a
+    name from KERNEL_KINDS or its index)."""
+    k = KERNEL_KINDS.index(kind) if isinstance(kind, str) else int(kind)
+    _check("attn_debug_inject_timeout", lib().attn_debug_inject_timeout(ctx, k))
 
 
 def attn_decode_attention_noalloc(q_r, cache_k, cache_v, B, kv_len, S_max, h, stream=None):

@@ -105,7 +105,9 @@ __global__ void __launch_bounds__(160)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       int issued = 0;
-      for (int i = 0; i < my_tiles; ++i) {
+      // test hook: CTA (0, 0, 0) issues no loads, so its consumers wait out and abort
+      const bool no_loads = p.fault && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+      for (int i = 0; i < (no_loads ? 0 : my_tiles); ++i) {
         const int s = i % kDecStages;
         const uint32_t ph = (i / kDecStages) & 1;
         if (!mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.status)) break;

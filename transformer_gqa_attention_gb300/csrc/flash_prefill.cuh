@@ -99,14 +99,15 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       griddep_wait();  // Q_r, K_r, V come from the projection kernel
-      mbar_arrive_expect_tx(q_full, 2 * L::kTile);
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
+      // test hook: CTA (0, 0) issues no loads, so its consumers wait out and abort
+      const bool no_loads = p.fault && blockIdx.x == 0 && blockIdx.y == 0;
+      if (!no_loads) mbar_arrive_expect_tx(q_full, 2 * L::kTile);
+      for (int i = 0; i < (no_loads ? 0 : 2); ++i) {
         tma_load_3d(smem + L::kQ + i * L::kTile, &tmQ, q_full, (h0 + i) * 128, q0, b);
         tma_load_3d(smem + L::kQ + i * L::kTile + L::kHalf, &tmQ, q_full, (h0 + i) * 128 + 64, q0, b);
       }
       int issued_k = 0, issued_v = 0;
-      for (int j = 0; j < n_kv; ++j) {
+      for (int j = 0; j < (no_loads ? 0 : n_kv); ++j) {
         const int st = j & 1;
         const uint32_t ph = (j >> 1) & 1;
         if (!mbar_wait(&k_empty[st], ph ^ 1u, abort_flag, p.status)) break;
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(384, 1)
         tma_load_4d(vd + L::kHalf, &tmV, &v_full[st], 64, g, j * 128, b);
         ++issued_v;
       }
-      if (*abort_flag) {  // let copies still in flight land before the CTA leaves
+      if (*abort_flag && !no_loads) {  // let copies still in flight land before the CTA leaves
         mbar_wait_drain(q_full, 0);
         for (int j = (issued_k > 2 ? issued_k - 2 : 0); j < issued_k; ++j)
           mbar_wait_drain(&k_full[j & 1], (j >> 1) & 1);

@@ -164,7 +164,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       bool ok = true;
       // B is the context's weight copy (never written after creation): its first stages are
       // fetched before waiting for the previous kernel; A (activations) only after.
-      const int n_pre = (pair < total_units) ? min(STAGES, p.num_kb) : 0;
+      // test hook: pair 0 issues no loads, so CTA 0's issuer waits out and aborts
+      const bool no_loads = p.fault && pair == 0;
+      const int n_pre = (pair < total_units && !no_loads) ? min(STAGES, p.num_kb) : 0;
       if (n_pre > 0) {
         const int n0 = (pair % p.n_tiles) * 256 + 128 * rank;
         for (int i = 0; i < n_pre; ++i) {
@@ -173,7 +175,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
       }
       griddep_wait();
-      for (int u = pair; ok && u < total_units; u += n_pairs) {
+      for (int u = pair; ok && !no_loads && u < total_units; u += n_pairs) {
         const int m0 = (u / p.n_tiles) * 256 + 128 * rank;
         const int n0 = (u % p.n_tiles) * 256 + 128 * rank;
         for (int i = 0; i < p.num_kb; ++i, ++it) {
@@ -334,14 +336,16 @@ __global__ void __launch_bounds__(192, 1)
       tma_prefetch_desc(&tmB);
       // A is the context's weight copy (never written after creation): its first stages are
       // fetched before waiting for the previous kernel; B (activations) only after.
-      const int n_pre = min(STAGES, nkb);
+      // test hook: cluster 0 issues no loads, so its issuers wait out and abort
+      const bool no_loads = p.fault && static_cast<int>(blockIdx.x) < p.splits;
+      const int n_pre = no_loads ? 0 : min(STAGES, nkb);
       for (int i = 0; i < n_pre; ++i) {
         mbar_arrive_expect_tx(&full_bar[i], L::kStageBytes);
         tma_load_3d(sA + i * L::kABytes, &tmA, &full_bar[i], 0, m0, kb0 + i);
       }
       griddep_wait();
       int issued = 0;
-      for (int i = 0; i < nkb; ++i) {
+      for (int i = 0; i < (no_loads ? 0 : nkb); ++i) {
         const int s = i % STAGES;
         if (i >= n_pre) {
           if (!mbar_wait(&empty_bar[s], ((i / STAGES) & 1) ^ 1u, abort_flag, p.status)) break;

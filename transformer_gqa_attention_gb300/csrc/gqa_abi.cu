@@ -36,6 +36,7 @@ struct gqa_ctx {
   std::vector<cudaEvent_t> ev;        // 2 per recorded launch
   std::vector<int> ev_kind;           // kind of each recorded launch
   size_t ev_used = 0;                 // launches recorded so far
+  int fault_kind = -1;                // test hook armed by attn_debug_inject_timeout
 };
 
 namespace {
@@ -221,6 +222,13 @@ gqa_status check_device(gqa_ctx* c) {
   return GQA_OK;
 }
 
+// One-shot test hook: 1 if the next launch of `kind` should skip its first unit's loads.
+int take_fault(gqa_ctx* c, int kind) {
+  if (c->fault_kind != kind) return 0;
+  c->fault_kind = -1;
+  return 1;
+}
+
 constexpr size_t kMaxProfiledLaunches = 65536;
 
 // RAII bracket of one kernel launch with two events when profiling is on.
@@ -277,6 +285,7 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
     p.fin2 = cv;
     p.R = R;
     const int grid = std::min(p.m_tiles * p.n_tiles * p.splits, 2 * c->num_sms);
+    p.fault = take_fault(c, GQA_KERNEL_QKV_SPLITK);
     { ProfScope ps(c, GQA_KERNEL_QKV_SPLITK, s); GQA_CUDA(launch_gemm_splitk_qkv(ta, tb, p, grid, s)); }
   } else {
     // CTA pairs, 256x256 tiles: each CTA loads 128-row boxes of x and of W_QKV
@@ -293,6 +302,7 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
     p.out2 = cv;
     p.R = R;
     const int grid = 2 * std::min(p.m_tiles * p.n_tiles, c->pair_clusters);
+    p.fault = take_fault(c, GQA_KERNEL_QKV_GEMM);
     { ProfScope ps(c, GQA_KERNEL_QKV_GEMM, s); GQA_CUDA(launch_gemm_qkv_rope(ta, tb, p, grid, s)); }
   }
   return GQA_OK;
@@ -316,6 +326,7 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
     p.m_tiles = 32;
     p.fin0 = delta;
     const int grid = std::min(p.m_tiles * p.n_tiles * p.splits, 2 * c->num_sms);
+    p.fault = take_fault(c, GQA_KERNEL_OUT_SPLITK);
     { ProfScope ps(c, GQA_KERNEL_OUT_SPLITK, s); GQA_CUDA(launch_gemm_splitk_out(ta, tb, p, grid, s)); }
   } else {
     if (!map_rows_k4096(&ta, h, n_tok, 128) || !map_weight_tiled(&tb, c->w_o, 4096, 128))
@@ -329,6 +340,7 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
     p.out0 = delta;
     p.ldo = 4096;
     const int grid = 2 * std::min(p.m_tiles * p.n_tiles, c->pair_clusters);
+    p.fault = take_fault(c, GQA_KERNEL_OUT_GEMM);
     { ProfScope ps(c, GQA_KERNEL_OUT_GEMM, s); GQA_CUDA(launch_gemm_store_f32(ta, tb, p, grid, s)); }
   }
   return GQA_OK;
@@ -444,6 +456,7 @@ gqa_status attn_prefill(gqa_ctx* c, const void* x, int B, int T, const float* R,
   fp.H = h;
   fp.status = c->status;
   fp.scale_log2 = kScaleLog2;
+  fp.fault = take_fault(c, GQA_KERNEL_FLASH_PREFILL);
   // grid.x = (b, head pair), grid.y = query tiles
   { ProfScope ps(c, GQA_KERNEL_FLASH_PREFILL, s); GQA_CUDA(launch_flash_prefill(tq, tk, tv, fp, dim3(B * 16, fp.n_qtiles), s)); }
 
@@ -494,6 +507,7 @@ gqa_status attn_decode(gqa_ctx* c, const void* x, int B, int start_pos, const fl
   p.status = c->status;
   p.scale_log2 = kScaleLog2;
   p.counters = c->counters;  // the last split of each (b, g) merges
+  p.fault = take_fault(c, GQA_KERNEL_DECODE_ATTN);
   { ProfScope ps(c, GQA_KERNEL_DECODE_ATTN, s); GQA_CUDA(launch_decode_attn(tk, tv, p, dim3(dp.n_splits, 8, B), s)); }
 
   // step 14
@@ -520,6 +534,22 @@ gqa_status attn_debug_buffers(gqa_ctx* c, const void** q_r, const void** h) {
   if (q_r) *q_r = c->last_q;
   if (h) *h = c->last_h;
   return GQA_OK;
+}
+
+gqa_status attn_debug_inject_timeout(gqa_ctx* c, int kind) {
+  if (!c) return GQA_ERR_INVALID_ARG;
+  switch (kind) {
+    case GQA_KERNEL_QKV_GEMM:
+    case GQA_KERNEL_QKV_SPLITK:
+    case GQA_KERNEL_FLASH_PREFILL:
+    case GQA_KERNEL_DECODE_ATTN:
+    case GQA_KERNEL_OUT_GEMM:
+    case GQA_KERNEL_OUT_SPLITK:
+      c->fault_kind = kind;
+      return GQA_OK;
+    default:
+      return GQA_ERR_INVALID_ARG;
+  }
 }
 
 gqa_status attn_profile_begin(gqa_ctx* c) {

@@ -35,6 +35,7 @@ struct GemmParams {
   void* fin1;        // kSplitKQkv: cache_k
   void* fin2;        // kSplitKQkv: cache_v
   int* status;
+  int fault;         // test hook: the first work unit's producer issues no loads (its waits run out)
 };
 
 struct FlashParams {
@@ -42,6 +43,7 @@ struct FlashParams {
   int n_qtiles;
   void* H;  // [B*T, 4096] bf16
   int* status;
+  int fault;  // test hook: CTA (0, 0)'s producer issues no loads (its waits run out)
   float scale_log2;  // log2(e) / sqrt(128)
 };
 
@@ -56,6 +58,7 @@ struct DecodeParams {
   int* counters;           // [B*8] arrival counters: the last split merges (null: separate merge kernel)
   void* H;        // [B, 4096] bf16 (combine output)
   int* status;
+  int fault;      // test hook: CTA (0, 0, 0)'s producer issues no loads (its waits run out)
   float scale_log2;
 };
 
