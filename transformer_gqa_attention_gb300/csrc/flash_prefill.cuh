@@ -239,14 +239,14 @@ __global__ void __launch_bounds__(384, 1)
         for (int i = 0; i < 128; ++i)
           if (key0 + i > lim) sv[i] = __float_as_uint(-INFINITY);
       }
-      // Row max as 8 independent chains (max is exact in any order).
+      // Row max: 8 independent chains of 3-input max (max is exact in any order).
       float m8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(sv[i]);
 #pragma unroll
-      for (int i = 8; i < 128; ++i) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(sv[i]));
-      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      for (int t = 0; t < 60; ++t)
+        m8[t & 7] = max3f(m8[t & 7], __uint_as_float(sv[8 + 2 * t]), __uint_as_float(sv[9 + 2 * t]));
+      const float mx = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       const float m_tile = mx * p.scale_log2;
       // Per-row lazy rescale decision (rows never influence each other's bits).
       float alpha = 1.f;
@@ -261,9 +261,11 @@ __global__ void __launch_bounds__(384, 1)
       }
       const float mu = (m_used == -INFINITY) ? 0.f : m_used;
       // P = exp2(s * scale_log2 - m_used), bf16, written over S_i in TMEM in two halves
-      // (keys 0..63, then 64..127), each released as soon as it is stored; the row sum
-      // accumulates in 8 independent partial sums.
-      float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // (keys 0..63, then 64..127), each released as soon as it is stored; scale and shift
+      // run as packed fp32 pairs and the row sum accumulates in 4 packed partial sums.
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+      const float2 nmu2 = make_float2(-mu, -mu);
+      float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
@@ -271,10 +273,11 @@ __global__ void __launch_bounds__(384, 1)
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c * 32 + 2 * e]), p.scale_log2, -mu));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c * 32 + 2 * e + 1]), p.scale_log2, -mu));
-            l8[e & 7] += p0 + p1;
-            w[e] = pack_bf16x2(p0, p1);
+            const float2 a = ffma2(make_float2(__uint_as_float(sv[c * 32 + 2 * e]), __uint_as_float(sv[c * 32 + 2 * e + 1])),
+                                   sc2, nmu2);
+            const float2 pe = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+            l4[e & 3] = fadd2(l4[e & 3], pe);
+            w[e] = pack_bf16x2(pe.x, pe.y);
           }
           tmem_st16(t_s + c * 16, w);
         }
@@ -295,7 +298,8 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_before();
         mbar_arrive(hf == 0 ? &p_lo[slot] : &p_hi[slot]);
       }
-      l_sum += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+      const float2 l2 = fadd2(fadd2(l4[0], l4[1]), fadd2(l4[2], l4[3]));
+      l_sum += l2.x + l2.y;
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[slot], 0, abort_flag, p.status));
     if (ok) {
