@@ -132,81 +132,92 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------------------------------------------------------- UMMA issuer
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);   // Q, K both K-major
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, 0, 1);  // P (TMEM), V MN-major
-      const uint32_t q_addr = smem_u32(smem + L::kQ);
-      const uint32_t k_addr = smem_u32(smem + L::kK);
-      const uint32_t v_addr = smem_u32(smem + L::kV);
-      // S_i(j) = Q_i K_j^T
-      auto issue_s = [&](int i, int j) {
-        const int st = j & 1;
-        const uint32_t d_s = tmem_base + i * 128;
+    // ------------------------------------------------------------------ UMMA issuer
+    // The whole warp runs the loop (its waits are warp-uniform); one elected lane issues
+    // the MMAs and commits.
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);   // Q, K both K-major
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, 0, 1);  // P (TMEM), V MN-major
+    const uint32_t q_addr = smem_u32(smem + L::kQ);
+    const uint32_t k_addr = smem_u32(smem + L::kK);
+    const uint32_t v_addr = smem_u32(smem + L::kV);
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.status));
+    };
+    auto commit = [&](uint64_t* bar) {
+      if (elect_one_sync()) umma_commit(bar);
+      __syncwarp();
+    };
+    // S_i(j) = Q_i K_j^T
+    auto issue_s = [&](int i, int j) {
+      const uint32_t d_s = tmem_base + i * 128;
+      const uint64_t qd = sdesc_sw128(q_addr + i * L::kTile, 0, 1024);
+      const uint64_t kd = sdesc_sw128(k_addr + (j & 1) * L::kTile, 0, 1024);
+      if (elect_one_sync()) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kHalf + (kk & 3) * 32;
-          umma_ss(d_s, sdesc_sw128(q_addr + i * L::kTile + off, 0, 1024),
-                  sdesc_sw128(k_addr + st * L::kTile + off, 0, 1024), idesc_s, kk != 0);
+          const uint32_t off = ((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4;  // descriptor address units
+          umma_ss(d_s, qd + off, kd + off, idesc_s, kk != 0);
         }
         umma_commit(&s_full[i]);
-      };
-      // O_i += P_i(j) V_j for keys 16*kk0 .. 16*kk0+63 (kk0 = 0 or 4); P_i holds keys
-      // (2c, 2c+1) in column c of S_i's TMEM columns.
-      auto issue_pv_half = [&](int i, int j, int kk0) {
-        const int st = j & 1;
-        const uint32_t d_o = tmem_base + 256 + i * 128;
-        const uint32_t a_p = tmem_base + i * 128;
+      }
+      __syncwarp();
+    };
+    // O_i += P_i(j) V_j for keys 16*kk0 .. 16*kk0+63 (kk0 = 0 or 4); P_i holds keys
+    // (2c, 2c+1) in column c of S_i's TMEM columns.  V: MN-major (d contiguous); 16 keys =
+    // two 8-row groups = 2048 B per step; d 64..127 lives in the second half (LBO), 8-key
+    // groups 1024 B apart (SBO).
+    auto issue_pv_half = [&](int i, int j, int kk0) {
+      const uint32_t d_o = tmem_base + 256 + i * 128;
+      const uint32_t a_p = tmem_base + i * 128;
+      const uint64_t vd = sdesc_sw128(v_addr + (j & 1) * L::kTile, L::kHalf, 1024);
+      if (elect_one_sync()) {
 #pragma unroll
-        for (int kk = kk0; kk < kk0 + 4; ++kk) {
-          // V: MN-major (d contiguous); 16 keys = two 8-row groups = 2048 B per step;
-          // d 64..127 lives in the second half (LBO), 8-key groups 1024 B apart (SBO).
-          umma_ts(d_o, a_p + kk * 8, sdesc_sw128(v_addr + st * L::kTile + kk * 2048, L::kHalf, 1024),
-                  idesc_pv, (j | kk) != 0);
-        }
-      };
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
-      if (ok) ok = mbar_wait(&k_full[0], 0, abort_flag, p.status);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        issue_s(1, 0);
-        umma_commit(&k_empty[0]);
+        for (int kk = kk0; kk < kk0 + 4; ++kk)
+          umma_ts(d_o, a_p + kk * 8, vd + ((kk * 2048) >> 4), idesc_pv, (j | kk) != 0);
       }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const bool more = j + 1 < n_kv;
-        // head slot 0: PV_0(j) in two halves as P arrives, then S_0(j+1)
-        if (!(ok = mbar_wait(&v_full[j & 1], (j >> 1) & 1, abort_flag, p.status))) break;
-        if (!(ok = mbar_wait(&p_lo[0], j & 1, abort_flag, p.status))) break;
+      __syncwarp();
+    };
+    bool ok = wait(q_full, 0);
+    if (ok) ok = wait(&k_full[0], 0);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0, 0);
+      issue_s(1, 0);
+      commit(&k_empty[0]);
+    }
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const bool more = j + 1 < n_kv;
+      // head slot 0: PV_0(j) in two halves as P arrives, then S_0(j+1)
+      if (!(ok = wait(&v_full[j & 1], (j >> 1) & 1))) break;
+      if (!(ok = wait(&p_lo[0], j & 1))) break;
+      tc_fence_after();
+      issue_pv_half(0, j, 0);
+      if (!(ok = wait(&p_hi[0], j & 1))) break;
+      tc_fence_after();
+      issue_pv_half(0, j, 4);
+      if (!more) commit(&o_full[0]);
+      if (more) {
+        if (!(ok = wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1))) break;
         tc_fence_after();
-        issue_pv_half(0, j, 0);
-        if (!(ok = mbar_wait(&p_hi[0], j & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        issue_pv_half(0, j, 4);
-        if (!more) umma_commit(&o_full[0]);
-        if (more) {
-          if (!(ok = mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_flag, p.status))) break;
-          tc_fence_after();
-          issue_s(0, j + 1);
-        }
-        // head slot 1: PV_1(j), then S_1(j+1)
-        if (!(ok = mbar_wait(&p_lo[1], j & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        issue_pv_half(1, j, 0);
-        if (!(ok = mbar_wait(&p_hi[1], j & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        issue_pv_half(1, j, 4);
-        umma_commit(&v_empty[j & 1]);
-        if (!more) umma_commit(&o_full[1]);
-        if (more) {
-          issue_s(1, j + 1);
-          umma_commit(&k_empty[(j + 1) & 1]);
-        }
+        issue_s(0, j + 1);
       }
-      if (*abort_flag) {  // let issued UMMAs finish before TMEM is released
-        umma_commit(drain);
-        mbar_wait_drain(drain, 0);
+      // head slot 1: PV_1(j), then S_1(j+1)
+      if (!(ok = wait(&p_lo[1], j & 1))) break;
+      tc_fence_after();
+      issue_pv_half(1, j, 0);
+      if (!(ok = wait(&p_hi[1], j & 1))) break;
+      tc_fence_after();
+      issue_pv_half(1, j, 4);
+      commit(&v_empty[j & 1]);
+      if (!more) commit(&o_full[1]);
+      if (more) {
+        issue_s(1, j + 1);
+        commit(&k_empty[(j + 1) & 1]);
       }
+    }
+    if (__any_sync(0xffffffffu, *abort_flag != 0)) {  // let issued UMMAs finish before TMEM is released
+      commit(drain);
+      mbar_wait_drain(drain, 0);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax

@@ -25,6 +25,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 __device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31) == 0; }
 
+// One lane of a converged warp (elect.sync over the full mask; with all 32 lanes active
+// the same lane is chosen every time, so tcgen05.commit tracks that lane's MMAs).
+__device__ __forceinline__ bool elect_one_sync() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ------------------------------------------------------------------------ dependent launch
 // Programmatic dependent launch: a kernel launched with programmatic stream serialization
 // may start before its predecessor on the stream has finished.  griddep_wait() blocks the
