@@ -201,8 +201,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
+    if (rank == 0) {
       // ------------------------------------------------------------ UMMA issuer (CTA 0)
+      // The whole warp runs the loop (waits are warp-uniform); one elected lane issues.
       constexpr uint32_t idesc = idesc_bf16_f32(256, 256, 0, 0);
       const uint32_t a_base = smem_u32(sA);
       const uint32_t b_base = smem_u32(sB);
@@ -210,29 +211,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       bool ok = true;
       for (int u = pair; ok && u < total_units; u += n_pairs, ++lt) {
         const int ab = lt & 1;
-        if (!mbar_wait_cluster(&acc_empty[ab], ((lt >> 1) & 1) ^ 1u, abort_flag, p.status)) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait_cluster(&acc_empty[ab], ((lt >> 1) & 1) ^ 1u, abort_flag,
+                                                             p.status))))
+          break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + ab * 256;
         for (int i = 0; i < p.num_kb; ++i, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(&full_bar[s], ph, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full_bar[s], ph, abort_flag, p.status)))) break;
           tc_fence_after();
+          const uint64_t da = sdesc_sw128(a_base + s * L::kABytes, 0, 1024);
+          const uint64_t db = sdesc_sw128(b_base + s * L::kBBytes, 0, 1024);
+          if (elect_one_sync()) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t da = sdesc_sw128(a_base + s * L::kABytes + k * 32, 0, 1024);
-            const uint64_t db = sdesc_sw128(b_base + s * L::kBBytes + k * 32, 0, 1024);
-            umma_ss_pair(d_tmem, da, db, idesc, (i | k) != 0);
+            for (int k = 0; k < 4; ++k) umma_ss_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (i | k) != 0);
+            umma_commit_pair(&empty_bar[s], 0x3);
           }
-          umma_commit_pair(&empty_bar[s], 0x3);
+          __syncwarp();
         }
-        if (ok) umma_commit_pair(&acc_full[ab], 0x3);
+        if (ok) {
+          if (elect_one_sync()) umma_commit_pair(&acc_full[ab], 0x3);
+          __syncwarp();
+        }
       }
-      if (*abort_flag) {  // let issued UMMAs finish before TMEM is released
-        umma_commit_pair(drain, 0x1);
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) {  // let issued UMMAs finish before TMEM is released
+        if (elect_one_sync()) umma_commit_pair(drain, 0x1);
+        __syncwarp();
         mbar_wait_drain(drain, 0);
       }
     }
@@ -361,24 +366,27 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, BN, 0, 0);
-      const uint32_t a_base = smem_u32(sA);
-      const uint32_t b_base = smem_u32(sB);
-      bool ok = true;
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % STAGES;
-        if (!(ok = mbar_wait(&full_bar[s], (i / STAGES) & 1, abort_flag, p.status))) break;
-        tc_fence_after();
+    // the whole warp runs the loop (waits are warp-uniform); one elected lane issues
+    constexpr uint32_t idesc = idesc_bf16_f32(128, BN, 0, 0);
+    const uint32_t a_base = smem_u32(sA);
+    const uint32_t b_base = smem_u32(sB);
+    bool ok = true;
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % STAGES;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full_bar[s], (i / STAGES) & 1, abort_flag, p.status)))) break;
+      tc_fence_after();
+      const uint64_t da = sdesc_sw128(a_base + s * L::kABytes, 0, 1024);
+      const uint64_t db = sdesc_sw128(b_base + s * L::kBBytes, 0, 1024);
+      if (elect_one_sync()) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma_ss(tmem_base, sdesc_sw128(a_base + s * L::kABytes + k * 32, 0, 1024),
-                  sdesc_sw128(b_base + s * L::kBBytes + k * 32, 0, 1024), idesc, (i | k) != 0);
+        for (int k = 0; k < 4; ++k) umma_ss(tmem_base, da + 2 * k, db + 2 * k, idesc, (i | k) != 0);
         umma_commit(&empty_bar[s]);
       }
-      umma_commit(ok ? acc_full : drain);
-      if (!ok) mbar_wait_drain(drain, 0);
+      __syncwarp();
     }
+    if (elect_one_sync()) umma_commit(ok ? acc_full : drain);
+    __syncwarp();
+    if (!ok) mbar_wait_drain(drain, 0);
   } else {
     // accumulator rows (features) -> this CTA's partial tile in shared memory
     const int quarter = warp & 3;
