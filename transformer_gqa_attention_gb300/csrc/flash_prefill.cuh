@@ -92,7 +92,11 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem_base = *tmem_holder;
   griddep_launch_dependents();
 
-  if (warp == 0) {
+  // registers: 168 x 384 at launch >= 72 x 128 (producer / issuer warpgroup) + 208 x 256
+  // (the two softmax warpgroups)
+  if (warp < 4) {
+   setmaxnreg_dec<72>();
+   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- producer
       tma_prefetch_desc(&tmQ);
@@ -131,7 +135,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_wait_drain(&v_full[j & 1], (j >> 1) & 1);
       }
     }
-  } else if (warp == 1) {
+   } else if (warp == 1) {
     // ------------------------------------------------------------------ UMMA issuer
     // The whole warp runs the loop (its waits are warp-uniform); one elected lane issues
     // the MMAs and commits.
@@ -219,7 +223,9 @@ __global__ void __launch_bounds__(384, 1)
       commit(drain);
       mbar_wait_drain(drain, 0);
     }
-  } else if (warp >= 4) {
+   }
+  } else {
+    setmaxnreg_inc<208>();
     // ------------------------------------------------------------------ softmax
     const int slot = (warp - 4) >> 2;  // head slot 0 or 1
     const int quarter = warp & 3;

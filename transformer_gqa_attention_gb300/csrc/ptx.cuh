@@ -25,6 +25,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 __device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31) == 0; }
 
+// Per-warpgroup register budget (all four warps of a warpgroup execute the same one).
+// An increase waits until other warpgroups have released enough of the registers the
+// block was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // One lane of a converged warp (elect.sync over the full mask; with all 32 lanes active
 // the same lane is chosen every time, so tcgen05.commit tracks that lane's MMAs).
 __device__ __forceinline__ bool elect_one_sync() {
