@@ -39,48 +39,97 @@ struct GemmSmem {
   static constexpr int kBytes = kBarOffset + 256 + 1024;  // + barriers + alignment slack
 };
 
-// Transform and store 32 accumulator columns (col0 .. col0+31) of output row m.
-template <int EPI>
-__device__ __forceinline__ void gemm_epilogue_chunk(const GemmParams& p, int m, int col0, int split,
-                                                    const uint32_t (&v)[32]) {
-  if (m >= p.M) return;
-  if constexpr (EPI == kQkvRope) {
-    const int b = m / p.T;
-    const int t = m - b * p.T;
-    const bool is_v = col0 >= 5120;
-    uint32_t w[16];
+// Epilogue of 32 x 32 chunks held by a warp (lane i = output row m_base + i).  A chunk goes
+// through a per-warp shared-memory tile (32 rows, stride 36 floats: conflict-free 16-byte
+// writes and reads) so that global stores and the RoPE table reads cover contiguous row
+// segments instead of one 16-byte piece of 32 rows each.
+constexpr int kEpiStride = 36;
+constexpr int kEpiWarpFloats = 32 * kEpiStride;
+
+__device__ __forceinline__ void stage_chunk(float* stage, int lane, const uint32_t (&v)[32]) {
+  float4* srow = reinterpret_cast<float4*>(stage + lane * kEpiStride);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    srow[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                          __uint_as_float(v[4 * i + 3]));
+}
+
+// Rows of the Q/K/V epilogue after the transpose: pass k (0..3) of a lane handles row
+// 8k + lane/4 of the warp's 32 rows, columns 8 (lane & 3) .. +7 of the chunk.
+struct QkvRows {
+  int m[4], b[4], t[4];
+};
+
+__device__ __forceinline__ QkvRows qkv_rows(const GemmParams& p, int lane, int m_base) {
+  QkvRows q;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    q.m[k] = m_base + 8 * k + (lane >> 2);
+    const int mc = min(q.m[k], p.M - 1);
+    q.b[k] = mc / p.T;
+    q.t[k] = mc - q.b[k] * p.T;
+  }
+  return q;
+}
+
+// (cos, sin) of the 4 RoPE pairs a lane rotates in chunk-column block cc (0..3) of a head
+// slice: pairs 16 cc + 4 (lane & 3) .. +3 of each of its 4 rows.
+__device__ __forceinline__ void load_rope(const GemmParams& p, const QkvRows& q, int lane, int cc,
+                                          float4 (&cs)[4][2]) {
+  const int j0 = 16 * cc + 4 * (lane & 3);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float4* rp = reinterpret_cast<const float4*>(p.R + (static_cast<size_t>(q.t[k]) * 64 + j0) * 2);
+    cs[k][0] = __ldg(rp);
+    cs[k][1] = __ldg(rp + 1);
+  }
+}
+
+// Q/K/V epilogue of one staged chunk (columns col0 .. col0+31, all of one of Q, K, V).
+__device__ __forceinline__ void store_qkv_chunk(const GemmParams& p, const float* stage, int lane, const QkvRows& q,
+                                                int col0, const float4 (&cs)[4][2]) {
+  const int cq = lane & 3;
+  const int col = col0 + 8 * cq;
+  const bool is_v = col0 >= 5120;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = 8 * k + (lane >> 2);
+    if (q.m[k] >= p.M) continue;
+    const float4 x0 = *reinterpret_cast<const float4*>(stage + r * kEpiStride + 8 * cq);
+    const float4 x1 = *reinterpret_cast<const float4*>(stage + r * kEpiStride + 8 * cq + 4);
+    uint4 w;
     if (is_v) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+      w = make_uint4(pack_bf16x2(x0.x, x0.y), pack_bf16x2(x0.z, x0.w), pack_bf16x2(x1.x, x1.y),
+                     pack_bf16x2(x1.z, x1.w));
     } else {
-      // pairs j0 .. j0+15 of this head slice
-      const int j0 = (col0 & 127) >> 1;
-      const float4* rp = reinterpret_cast<const float4*>(p.R + (static_cast<size_t>(t) * 64 + j0) * 2);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 cs = __ldg(rp + i);  // (cos, sin) of pairs 2i and 2i+1
-        const float e0 = __uint_as_float(v[4 * i + 0]), o0 = __uint_as_float(v[4 * i + 1]);
-        const float e1 = __uint_as_float(v[4 * i + 2]), o1 = __uint_as_float(v[4 * i + 3]);
-        w[2 * i + 0] = pack_bf16x2(cs.x * e0 - cs.y * o0, cs.y * e0 + cs.x * o0);
-        w[2 * i + 1] = pack_bf16x2(cs.z * e1 - cs.w * o1, cs.w * e1 + cs.z * o1);
-      }
+      const float4 c0 = cs[k][0], c1 = cs[k][1];  // (cos, sin) of two pairs per float4
+      w = make_uint4(pack_bf16x2(c0.x * x0.x - c0.y * x0.y, c0.y * x0.x + c0.x * x0.y),
+                     pack_bf16x2(c0.z * x0.z - c0.w * x0.w, c0.w * x0.z + c0.z * x0.w),
+                     pack_bf16x2(c1.x * x1.x - c1.y * x1.y, c1.y * x1.x + c1.x * x1.y),
+                     pack_bf16x2(c1.z * x1.z - c1.w * x1.w, c1.w * x1.z + c1.z * x1.w));
     }
     __nv_bfloat16* dst;
     if (col0 < 4096) {
-      dst = static_cast<__nv_bfloat16*>(p.out0) + static_cast<size_t>(m) * 4096 + col0;
+      dst = static_cast<__nv_bfloat16*>(p.out0) + static_cast<size_t>(q.m[k]) * 4096 + col;
     } else {
-      const size_t cache_row = static_cast<size_t>(b) * p.S_max + p.start_pos + t;
-      dst = static_cast<__nv_bfloat16*>(is_v ? p.out2 : p.out1) + cache_row * 1024 + (col0 - (is_v ? 5120 : 4096));
+      const size_t cache_row = static_cast<size_t>(q.b[k]) * p.S_max + p.start_pos + q.t[k];
+      dst = static_cast<__nv_bfloat16*>(is_v ? p.out2 : p.out1) + cache_row * 1024 + (col - (is_v ? 5120 : 4096));
     }
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    *reinterpret_cast<uint4*>(dst) = w;
+  }
+}
+
+// fp32 epilogue of one staged chunk: 8 passes of 4 rows, lane -> row 4k + lane/8, columns
+// col0 + 4 (lane & 7) .. +3.
+__device__ __forceinline__ void store_f32_chunk(const GemmParams& p, const float* stage, int lane, int m_base,
+                                                int col0) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-  } else if constexpr (EPI == kStoreF32) {
-    float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(p.out0) + static_cast<size_t>(m) * p.ldo + col0);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
-                          __uint_as_float(v[4 * i + 3]));
+  for (int k = 0; k < 8; ++k) {
+    const int r = 4 * k + (lane >> 3);
+    const int m = m_base + r;
+    if (m >= p.M) continue;
+    const float4 x = *reinterpret_cast<const float4*>(stage + r * kEpiStride + 4 * (lane & 7));
+    *reinterpret_cast<float4*>(static_cast<float*>(p.out0) + static_cast<size_t>(m) * p.ldo + col0 + 4 * (lane & 7)) = x;
   }
 }
 
@@ -101,7 +150,8 @@ struct GemmPairSmem {
   static constexpr int kBBytes = 128 * 64 * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kBarOffset = STAGES * kStageBytes;
-  static constexpr int kBytes = kBarOffset + 256 + 1024;
+  static constexpr int kEpiOffset = kBarOffset + 256;  // 4 epilogue warps' staging tiles
+  static constexpr int kBytes = kEpiOffset + 4 * kEpiWarpFloats * 4 + 1024;
   static constexpr int kTmemCols = 512;  // two 256-column accumulators
 };
 
@@ -225,7 +275,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           const uint64_t db = sdesc_sw128(b_base + s * L::kBBytes, 0, 1024);
           if (elect_one_sync()) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) umma_ss_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (i | k) != 0);
+            for (int k = 0; k < 4; ++k)
+              umma_ss_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (i | k) != 0);
             umma_commit_pair(&empty_bar[s], 0x3);
           }
           __syncwarp();
@@ -246,6 +297,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    float* stage = reinterpret_cast<float*>(smem + L::kEpiOffset) + (warp - 2) * kEpiWarpFloats;
     int lt = 0;
     for (int u = pair; u < total_units; u += n_pairs, ++lt) {
       const int ab = lt & 1;
@@ -253,14 +305,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + lane_off + ab * 256;
-      const int m = (u / p.n_tiles) * 256 + 128 * rank + row;
+      const int m_base = (u / p.n_tiles) * 256 + 128 * rank + quarter * 32;
       const int n0 = (u % p.n_tiles) * 256;
+      // chunks cp and cp + 4 (the tile's two 128-column head slices) share RoPE pairs; the
+      // next pair's table reads are issued before this pair is stored
+      const bool rope = EPI == kQkvRope && n0 < 5120;
+      QkvRows qr{};
+      float4 cs[4][2], cs_next[4][2];
+      if constexpr (EPI == kQkvRope) {
+        qr = qkv_rows(p, lane, m_base);
+        if (rope) load_rope(p, qr, lane, 0, cs);
+      }
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        uint32_t v[32];
-        tmem_ld32(t_row + c * 32, v);
+      for (int cp = 0; cp < 4; ++cp) {
+        if constexpr (EPI == kQkvRope) {
+          if (rope && cp < 3) load_rope(p, qr, lane, cp + 1, cs_next);
+        }
+        uint32_t va[32], vb[32];
+        tmem_ld32(t_row + cp * 32, va);
+        tmem_ld32(t_row + (cp + 4) * 32, vb);
         tmem_ld_wait();
-        gemm_epilogue_chunk<EPI>(p, m, n0 + c * 32, 0, v);
+        stage_chunk(stage, lane, va);
+        __syncwarp();
+        if constexpr (EPI == kQkvRope) {
+          store_qkv_chunk(p, stage, lane, qr, n0 + cp * 32, cs);
+        } else {
+          store_f32_chunk(p, stage, lane, m_base, n0 + cp * 32);
+        }
+        __syncwarp();
+        stage_chunk(stage, lane, vb);
+        __syncwarp();
+        if constexpr (EPI == kQkvRope) {
+          store_qkv_chunk(p, stage, lane, qr, n0 + (cp + 4) * 32, cs);
+        } else {
+          store_f32_chunk(p, stage, lane, m_base, n0 + (cp + 4) * 32);
+        }
+        __syncwarp();
+        if constexpr (EPI == kQkvRope) {
+          if (rope && cp < 3) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              cs[k][0] = cs_next[k][0];
+              cs[k][1] = cs_next[k][1];
+            }
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
