@@ -382,19 +382,27 @@ __global__ void __launch_bounds__(192, 1)
                                const GemmParams p) {
   constexpr int BN = 64;
   using L = GemmSmem<BN, STAGES>;
-  static_assert(STAGES * L::kStageBytes >= 64 * 128 * 4, "partial tile must fit in the stage buffers");
+  // after the main loop the stage buffers hold this CTA's partial tile, token-major
+  // [64 tokens][128 features] fp32, then the receive slots: per source rank the rows of the
+  // tokens this CTA reduces (at most 32 when splits >= 2)
+  constexpr int kRecvTokens = 32;
+  constexpr int kPartBytes = BN * 128 * 4;
+  constexpr int kRecvSlotBytes = kRecvTokens * 128 * 4;
+  static_assert(STAGES * L::kStageBytes >= kPartBytes + 8 * kRecvSlotBytes, "partials must fit in the stage buffers");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
 
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * L::kABytes;
-  float* red = reinterpret_cast<float*>(smem);  // [64][128] partial tile, after the main loop
+  float* red = reinterpret_cast<float*>(smem);                // [64 tokens][128] partial tile
+  float* recv = reinterpret_cast<float*>(smem + kPartBytes);  // [source rank][kRecvTokens][128]
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* acc_full = empty_bar + STAGES;
   uint64_t* drain = acc_full + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* recv_bar = drain + 1;  // completes when every peer's rows for this CTA have landed
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(recv_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -411,6 +419,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(acc_full, 1);
     mbar_init(drain, 1);
+    mbar_init(recv_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -423,6 +432,13 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   griddep_launch_dependents();
+
+  // CTA r reduces tokens [r N / splits, (r+1) N / splits); its recv_bar expects those rows
+  // from every other split
+  const int t_lo = split * p.N / p.splits;
+  const int t_hi = (split + 1) * p.N / p.splits;
+  if (threadIdx.x == 64)
+    mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((p.splits - 1) * (t_hi - t_lo)) * 512u);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -477,9 +493,9 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
     if (!ok) mbar_wait_drain(drain, 0);
   } else {
-    // accumulator rows (features) -> this CTA's partial tile in shared memory
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
+    // accumulator rows (features) -> this CTA's partial tile in shared memory
     if (bar1_and_128(mbar_wait(acc_full, 0, abort_flag, p.status))) {
       tc_fence_after();
 #pragma unroll
@@ -490,6 +506,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) red[(c * 32 + i) * 128 + row] = __uint_as_float(v[i]);
       }
+      fence_proxy_async_smem();  // the bulk copies below read these rows
     }
   }
 
@@ -497,58 +514,78 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   cluster_sync();  // every split's partial tile is in its CTA's shared memory
 
-  if (warp >= 2 && !*abort_flag) {
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const int m = m0 + row;
-    const int t_lo = split * p.N / p.splits;
-    const int t_hi = (split + 1) * p.N / p.splits;
-    const uint32_t red_addr = smem_u32(red);
-    // 4 tokens per pass, all splits' loads issued before the sums are used
-    for (int tok0 = t_lo; tok0 < t_hi; tok0 += 4) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  // Every CTA pushes the rows of its partial tile that CTA d reduces into CTA d's receive
+  // slot with one bulk shared-to-shared copy, completing on CTA d's recv_bar; CTA d then sums
+  // from its own shared memory.  The copies are issued even after an abort (no TMA write is
+  // in flight past the barrier above), so every recv_bar completes and no CTA leaves while a
+  // copy into it is landing.
+  if (threadIdx.x == 64) {
+    for (int d = 0; d < p.splits; ++d) {
+      const int d_lo = d * p.N / p.splits;
+      const int d_hi = (d + 1) * p.N / p.splits;
+      if (d == split || d_hi == d_lo) continue;
+      bulk_copy_smem_to_cluster(mapa_shared(smem_u32(recv) + split * kRecvSlotBytes, d),
+                                smem_u32(red + d_lo * 128), static_cast<uint32_t>(d_hi - d_lo) * 512u,
+                                mapa_shared(smem_u32(recv_bar), d));
+    }
+  }
+  bool go = false;
+  if (warp >= 2) {
+    go = !*abort_flag;
+    if (go) {
+      go = mbar_wait(recv_bar, 0, abort_flag, p.status);
+    } else {
+      mbar_wait_drain(recv_bar, 0);
+    }
+    go = bar1_and_128(go);
+  }
+  if (go) {
+    // Warp w of the four epilogue warps takes tokens t_lo + w, t_lo + w + 4, ...; lane l takes
+    // features 4l .. 4l+3 of the CTA's 128 (two RoPE pairs), so every shared load is a
+    // conflict-free 16-byte read and one warp store writes a token's whole 128-feature row.
+    const int ew = warp - 2;
+    const int f0 = 4 * lane;
+    const int m = m0 + f0;
+    const bool rope = EPI == kSplitKQkv && m < 5120;
+#pragma unroll 2
+    for (int tok = t_lo + ew; tok < t_hi; tok += 4) {
+      float4 acc = *reinterpret_cast<const float4*>(red + tok * 128 + f0);
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
-        if (r < p.splits) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int tok = min(tok0 + q, t_hi - 1);
-            acc[q] += ld_shared_cluster_f32(mapa_shared(red_addr + (tok * 128 + row) * 4, r));
-          }
+        if (r < p.splits && r != split) {
+          const float4 v = *reinterpret_cast<const float4*>(recv + (r * kRecvTokens + tok - t_lo) * 128 + f0);
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
         }
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int tok = tok0 + q;
-        if (tok >= t_hi) break;
-        if constexpr (EPI == kSplitKOut) {
-          static_cast<float*>(p.fin0)[static_cast<size_t>(tok) * 4096 + m] = acc[q];
+      if constexpr (EPI == kSplitKOut) {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.fin0) + static_cast<size_t>(tok) * 4096 + m) = acc;
+      } else {
+        const int b = tok / p.T;
+        const int t = tok - b * p.T;
+        if (rope) {
+          // (cos, sin) of pairs (m & 127) / 2 and the next one
+          const float4 cs = __ldg(reinterpret_cast<const float4*>(p.R + (static_cast<size_t>(t) * 64 + ((m & 127) >> 1)) * 2));
+          const float e0 = acc.x, o0 = acc.y, e1 = acc.z, o1 = acc.w;
+          acc = make_float4(cs.x * e0 - cs.y * o0, cs.y * e0 + cs.x * o0, cs.z * e1 - cs.w * o1, cs.w * e1 + cs.z * o1);
+        }
+        const uint2 o = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+        if (m < 4096) {
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.fin0) + static_cast<size_t>(tok) * 4096 + m) = o;
         } else {
-          // rotation pairs (2j, 2j+1) are held by adjacent lanes
-          const float partner = __shfl_xor_sync(0xffffffffu, acc[q], 1);
-          const int b = tok / p.T;
-          const int t = tok - b * p.T;
-          float outv = acc[q];
-          if (m < 5120) {
-            const float2 cs =
-                __ldg(reinterpret_cast<const float2*>(p.R) + static_cast<size_t>(t) * 64 + ((m & 127) >> 1));
-            outv = (lane & 1) ? (cs.y * partner + cs.x * acc[q]) : (cs.x * acc[q] - cs.y * partner);
-          }
-          const __nv_bfloat16 o = __float2bfloat16_rn(outv);
-          if (m < 4096) {
-            static_cast<__nv_bfloat16*>(p.fin0)[static_cast<size_t>(tok) * 4096 + m] = o;
-          } else {
-            const bool is_v = m >= 5120;
-            const size_t crow = static_cast<size_t>(b) * p.S_max + p.start_pos + t;
-            static_cast<__nv_bfloat16*>(is_v ? p.fin2 : p.fin1)[crow * 1024 + (m - (is_v ? 5120 : 4096))] = o;
-          }
+          const bool is_v = m >= 5120;
+          const size_t crow = static_cast<size_t>(b) * p.S_max + p.start_pos + t;
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(is_v ? p.fin2 : p.fin1) + crow * 1024 +
+                                    (m - (is_v ? 5120 : 4096))) = o;
         }
       }
     }
   }
 
-  // no CTA leaves while its partial tile may still be read (the reads have completed once
-  // their values were summed, so no release ordering is needed)
+  // no CTA leaves while a peer's copy out of its partial tile may be in flight (every copy
+  // has completed once its destination's recv_bar has, which each CTA waited for above)
   cluster_sync_relaxed();
   if (warp == 1) {
     tc_fence_after();

@@ -361,6 +361,18 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
   return v;
 }
 
+// Bulk copy of `bytes` (multiple of 16, 16-byte aligned) from this CTA's shared memory to a
+// shared::cluster address (a peer CTA's buffer); completes as transaction bytes on the
+// mbarrier at `bar_cluster_addr` (in the destination CTA).
+__device__ __forceinline__ void bulk_copy_smem_to_cluster(uint32_t dst_cluster_addr, uint32_t src_smem,
+                                                          uint32_t bytes, uint32_t bar_cluster_addr) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster_addr),
+      "r"(src_smem), "r"(bytes), "r"(bar_cluster_addr)
+      : "memory");
+}
+
 // Arrive on an mbarrier given by its shared::cluster address (possibly in the peer CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
