@@ -21,8 +21,8 @@ cudaError_t configure_kernels() {
 }
 
 cudaError_t launch_flash_prefill(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                 const FlashParams& p, dim3 grid, cudaStream_t s) {
-  return launch_pdl(flash_prefill_kernel, grid, dim3(384), FlashSmem::kBytes, s, 0, q, k, v, p);
+                                 const CUtensorMap& h, const FlashParams& p, dim3 grid, cudaStream_t s) {
+  return launch_pdl(flash_prefill_kernel, grid, dim3(384), FlashSmem::kBytes, s, 0, q, k, v, h, p);
 }
 
 cudaError_t launch_decode_attn(const CUtensorMap& k, const CUtensorMap& v, const DecodeParams& p,

@@ -44,7 +44,8 @@ struct FlashSmem {
 
 __global__ void __launch_bounds__(384, 1)
     flash_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, const FlashParams p) {
+                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmH,
+                         const FlashParams p) {
   using L = FlashSmem;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -320,26 +321,38 @@ __global__ void __launch_bounds__(384, 1)
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[slot], 0, abort_flag, p.status));
     if (ok) {
+      // O / l as bf16 into this slot's Q tile (free once the last UMMA has completed), in the
+      // 128-byte-swizzled layout the tile was loaded in: row r, 16-byte chunk c of a 64-column
+      // half at chunk position c ^ (r & 7) (conflict-free); then two TMA stores, which leave
+      // out the rows of a ragged last tile past T.
       tc_fence_after();
       const float inv_l = 1.f / l_sum;
-      const bool valid = (q0 + r) < p.T;
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.H) + (static_cast<size_t>(b) * p.T + q0 + r) * 4096 +
-                           (h0 + slot) * 128;
+      uint8_t* tile = smem + L::kQ + slot * L::kTile;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
         tmem_ld32(t_o + c * 32, v);
         tmem_ld_wait();
-        if (valid) {
-          uint32_t w[16];
+        uint8_t* row_base = tile + (c >> 1) * L::kHalf + r * 128;
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv_l, __uint_as_float(v[2 * i + 1]) * inv_l);
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        for (int k = 0; k < 4; ++k) {
+          const int chunk = (c & 1) * 4 + k;
+          const uint4 w4 = make_uint4(pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l),
+                                      pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l),
+                                      pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l),
+                                      pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l));
+          *reinterpret_cast<uint4*>(row_base + ((chunk ^ (r & 7)) << 4)) = w4;
         }
       }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(2 + slot, 128);
+    if (ok && quarter == 0 && lane == 0) {
+      const uint8_t* tile = smem + L::kQ + slot * L::kTile;
+      tma_store_3d(&tmH, tile, (h0 + slot) * 128, q0, b);
+      tma_store_3d(&tmH, tile + L::kHalf, (h0 + slot) * 128 + 64, q0, b);
+      tma_store_commit();
+      tma_store_wait_read();
     }
   }
 

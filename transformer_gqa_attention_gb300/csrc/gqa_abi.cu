@@ -437,12 +437,14 @@ gqa_status attn_prefill(gqa_ctx* c, const void* x, int B, int T, const float* R,
 
   // steps 6-13: causal GQA flash attention over keys 0 .. start_pos+T-1
   const int kv_len = start_pos + T;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, th;
   {
+    // Q_r (read) and H (written) are both [B, T, 4096] bf16, addressed in 64 x 128 boxes
     const uint64_t dims[3] = {4096, static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
     const uint64_t strides[2] = {4096 * 2, static_cast<uint64_t>(T) * 4096 * 2};
     const uint32_t box[3] = {64, 128, 1};
-    if (!make_map(&tq, q_r, 3, dims, strides, box) || !map_cache(&tk, cache_k, B, S_max, kv_len, 128) ||
+    if (!make_map(&tq, q_r, 3, dims, strides, box) || !make_map(&th, h, 3, dims, strides, box) ||
+        !map_cache(&tk, cache_k, B, S_max, kv_len, 128) ||
         !map_cache(&tv, cache_v, B, S_max, kv_len, 128))
       return cuda_fail(cudaErrorInvalidValue);
   }
@@ -458,7 +460,7 @@ gqa_status attn_prefill(gqa_ctx* c, const void* x, int B, int T, const float* R,
   fp.scale_log2 = kScaleLog2;
   fp.fault = take_fault(c, GQA_KERNEL_FLASH_PREFILL);
   // grid.x = (b, head pair), grid.y = query tiles
-  { ProfScope ps(c, GQA_KERNEL_FLASH_PREFILL, s); GQA_CUDA(launch_flash_prefill(tq, tk, tv, fp, dim3(B * 16, fp.n_qtiles), s)); }
+  { ProfScope ps(c, GQA_KERNEL_FLASH_PREFILL, s); GQA_CUDA(launch_flash_prefill(tq, tk, tv, th, fp, dim3(B * 16, fp.n_qtiles), s)); }
 
   return run_out(c, h, n_tok, delta, w, sk, s);
 }

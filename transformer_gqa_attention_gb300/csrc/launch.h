@@ -62,7 +62,7 @@ cudaError_t launch_gemm_splitk_out(const CUtensorMap& a, const CUtensorMap& b, c
                                    int grid, cudaStream_t s);
 
 cudaError_t launch_flash_prefill(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                 const FlashParams& p, dim3 grid, cudaStream_t s);
+                                 const CUtensorMap& h, const FlashParams& p, dim3 grid, cudaStream_t s);
 cudaError_t launch_decode_attn(const CUtensorMap& k, const CUtensorMap& v, const DecodeParams& p,
                                dim3 grid, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeParams& p, int B, cudaStream_t s);
