@@ -295,7 +295,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   } else {
     // -------------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-    const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     float* stage = reinterpret_cast<float*>(smem + L::kEpiOffset) + (warp - 2) * kEpiWarpFloats;
     int lt = 0;
