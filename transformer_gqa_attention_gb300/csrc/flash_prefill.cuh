@@ -68,11 +68,20 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const int b = blockIdx.x / 16;
-  const int hp = blockIdx.x % 16;
+  // Work order (1-D grid, dispatched in index order): bands of groups_per_band (sequence,
+  // kv group) pairs; within a band the heaviest query tiles first, across its groups and the
+  // group's two head pairs.  A band's K/V are sized to stay in L2 while its CTAs run.
+  const int band_ctas = p.groups_per_band * 2 * p.n_qtiles;
+  const int band = static_cast<int>(blockIdx.x) / band_ctas;
+  const int w_in = static_cast<int>(blockIdx.x) - band * band_ctas;
+  const int qi = w_in / (2 * p.groups_per_band);
+  const int gp = w_in - qi * 2 * p.groups_per_band;
+  const int grp = band * p.groups_per_band + (gp >> 1);  // b * 8 + kv group
+  const int b = grp >> 3;
+  const int hp = ((grp & 7) << 1) | (gp & 1);
   const int h0 = 2 * hp;
   const int g = h0 >> 2;
-  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.y);  // heaviest tiles first
+  const int qt = p.n_qtiles - 1 - qi;  // heaviest tiles first
   const int q0 = qt * 128;
   const int kv_len = p.start_pos + p.T;
   const int kv_hi = p.causal ? min(kv_len, p.start_pos + q0 + 128) : kv_len;
@@ -104,8 +113,8 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       griddep_wait();  // Q_r, K_r, V come from the projection kernel
-      // test hook: CTA (0, 0) issues no loads, so its consumers wait out and abort
-      const bool no_loads = p.fault && blockIdx.x == 0 && blockIdx.y == 0;
+      // test hook: CTA 0 issues no loads, so its consumers wait out and abort
+      const bool no_loads = p.fault && blockIdx.x == 0;
       if (!no_loads) mbar_arrive_expect_tx(q_full, 2 * L::kTile);
       for (int i = 0; i < (no_loads ? 0 : 2); ++i) {
         tma_load_3d(smem + L::kQ + i * L::kTile, &tmQ, q_full, (h0 + i) * 128, q0, b);

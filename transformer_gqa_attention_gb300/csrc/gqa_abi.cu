@@ -459,8 +459,19 @@ gqa_status attn_prefill(gqa_ctx* c, const void* x, int B, int T, const float* R,
   fp.status = c->status;
   fp.scale_log2 = kScaleLog2;
   fp.fault = take_fault(c, GQA_KERNEL_FLASH_PREFILL);
-  // grid.x = (b, head pair), grid.y = query tiles
-  { ProfScope ps(c, GQA_KERNEL_FLASH_PREFILL, s); GQA_CUDA(launch_flash_prefill(tq, tk, tv, th, fp, dim3(B * 16, fp.n_qtiles), s)); }
+  // Scheduling bands: all (sequence, kv group) pairs at once while their K/V (kv_len x 512 B
+  // each) total at most 64 MB; otherwise the largest power-of-two count of pairs dividing 8
+  // whose K/V fit in 32 MB, so the CTAs resident together reuse K/V tiles through L2.
+  {
+    const long long kv_bytes = static_cast<long long>(kv_len) * 512;
+    int gpb = 8 * B;
+    if (kv_bytes * gpb > (64LL << 20)) {
+      gpb = 8;
+      while (gpb > 1 && kv_bytes * gpb > (32LL << 20)) gpb >>= 1;
+    }
+    fp.groups_per_band = gpb;
+  }
+  { ProfScope ps(c, GQA_KERNEL_FLASH_PREFILL, s); GQA_CUDA(launch_flash_prefill(tq, tk, tv, th, fp, dim3(B * 16 * fp.n_qtiles), s)); }
 
   return run_out(c, h, n_tok, delta, w, sk, s);
 }

@@ -41,9 +41,10 @@ struct GemmParams {
 struct FlashParams {
   int B, T, S_max, start_pos, causal;
   int n_qtiles;
+  int groups_per_band;  // (sequence, kv group) pairs scheduled together (divides 8 B)
   void* H;  // [B*T, 4096] bf16
   int* status;
-  int fault;  // test hook: CTA (0, 0)'s producer issues no loads (its waits run out)
+  int fault;  // test hook: CTA 0's producer issues no loads (its waits run out)
   float scale_log2;  // log2(e) / sqrt(128)
 };
 
