@@ -188,6 +188,41 @@ def attention_decode(x, wq, wk, wv, wo, R_row, cache_k, cache_v, start_pos: int,
                            cache_k=cache_k, cache_v=cache_v, n_heads=n_heads, keep=keep)
 
 
+# --------------------------------------------------------------------------------------
+# Around the block.  The transformer block feeds the attention block attention_norm(x)
+# and adds its update back: h = x + Delta_attn (page "Llama 3.1 8B · Merge and project",
+# code excerpt model.py 236-248 and "Contextual evidence from Output projection").  The
+# RMSNorm body is not on the pages; its plainest reading, with the catalogue's
+# norm_eps = 1e-05 (sku_list.py arch_args on the same page), is
+#     attention_norm(x) = x / sqrt(mean_j x_j^2 + eps) * w      (per token row, j over dim)
+# --------------------------------------------------------------------------------------
+NORM_EPS = 1e-5
+
+
+def rms_norm(x, w, eps: float = NORM_EPS) -> np.ndarray:
+    x = f64(x)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * f64(w)
+
+
+def attention_block_residual(x, w_norm, wq, wk, wv, wo, R, *, eps: float = NORM_EPS, rows=None, **kw):
+    """h = x + Delta_attn(attention_norm(x)) for the residual stream x [B, T, dim].
+
+    Same keyword arguments as attention_block (causal, start_pos, caches, ...); returns
+    (h [B, len(rows), dim], extras)."""
+    x = f64(x)
+    delta, extras = attention_block(rms_norm(x, w_norm, eps), wq, wk, wv, wo, R, rows=rows, **kw)
+    xr = x if rows is None else x[:, np.asarray(rows, dtype=np.int64)]
+    return xr + delta, extras
+
+
+def attention_decode_residual(x, w_norm, wq, wk, wv, wo, R_row, cache_k, cache_v, start_pos: int, *,
+                              eps: float = NORM_EPS, n_heads: int = N_HEADS):
+    """Decode form of attention_block_residual (x [B, 1, dim])."""
+    return attention_block_residual(x, w_norm, wq, wk, wv, wo, R_row, eps=eps, causal=True,
+                                    start_pos=start_pos, cache_k=cache_k, cache_v=cache_v, n_heads=n_heads)
+
+
 def param_count(wq, wk, wv, wo) -> int:
     """Learned parameters of one block: the four projection matrices (no biases)."""
     return sum(math.prod(tuple(w.shape)) for w in (wq, wk, wv, wo))

@@ -378,3 +378,93 @@ def test_planted_missing_scale_is_caught(monkeypatch):
     _planted(monkeypatch, "softmax_rows", lambda Sm: orig_softmax(Sm * math.sqrt(2.0)))
     with pytest.raises(AssertionError):
         test_attention_core_equals_torch_sdpa_fp64(False)
+
+
+# ---------------------------------------------------------------- around the block
+def test_rms_norm_constant_row_closed_form():
+    # x = c * 1: mean x^2 = c^2, so y = w * c / sqrt(c^2 + eps) (a dropped eps, a sum instead
+    # of a mean or a missing weight all change this value)
+    c, eps = 0.003, 1e-5
+    w = np.linspace(0.5, 1.5, 64)
+    y = orc.rms_norm(np.full((1, 2, 64), c), w, eps)
+    np.testing.assert_allclose(y, np.broadcast_to(w * c / math.sqrt(c * c + eps), (1, 2, 64)), rtol=1e-14)
+
+
+def test_rms_norm_unit_rms_and_scale_invariance():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((3, 4, 128)) * 7.0
+    y = orc.rms_norm(x, np.ones(128), eps=0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, rtol=1e-13)  # per row
+    np.testing.assert_allclose(orc.rms_norm(2.5 * x, np.ones(128), eps=0.0), y, rtol=1e-13)
+    # rows are normalised independently
+    x2 = x.copy()
+    x2[0, 0] *= 100.0
+    y2 = orc.rms_norm(x2, np.ones(128), eps=0.0)
+    np.testing.assert_allclose(y2[0, 1:], y[0, 1:], rtol=1e-14)
+    np.testing.assert_allclose(y2[1:], y[1:], rtol=1e-14)
+
+
+def test_rms_norm_equals_loops_and_torch():
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((2, 3, 16))
+    w = rng.standard_normal(16)
+    eps = 1e-5
+    ref = np.empty_like(x)
+    for b in range(2):
+        for t in range(3):
+            ms = sum(v * v for v in x[b, t]) / 16
+            ref[b, t] = [x[b, t, j] / math.sqrt(ms + eps) * w[j] for j in range(16)]
+    np.testing.assert_allclose(orc.rms_norm(x, w, eps), ref, rtol=1e-13)
+    xt = torch.from_numpy(x)
+    tref = torch.nn.functional.rms_norm(xt, (16,), torch.from_numpy(w), eps) if hasattr(torch.nn.functional, "rms_norm") else None
+    if tref is not None:
+        np.testing.assert_allclose(orc.rms_norm(x, w, eps), tref.numpy(), rtol=1e-12)
+
+
+def test_residual_block_adds_update_to_unnormalised_input():
+    x, wq, wk, wv, wo, R = tiny(seed=21)
+    w_norm = np.random.default_rng(3).standard_normal(x.shape[-1]) * 0.2 + 1.0
+    h, _ = orc.attention_block_residual(x, w_norm, wq, wk, wv, wo, R, n_heads=8)
+    delta, _ = orc.attention_block(orc.rms_norm(x, w_norm), wq, wk, wv, wo, R, n_heads=8)
+    np.testing.assert_allclose(h, x + delta, rtol=1e-13, atol=1e-13)
+    # W_O = 0: the block is the identity on the residual stream
+    h0, _ = orc.attention_block_residual(x, w_norm, wq, wk, wv, np.zeros_like(wo), R, n_heads=8)
+    np.testing.assert_array_equal(h0, x)
+    # the update sees the normalised input: scaling a token row leaves its own update unchanged
+    # (eps aside) while the residual scales, i.e. h(c x)[t] - c x[t] == h(x)[t] - x[t] for T = 1
+    x1 = x[:, :1]
+    a, _ = orc.attention_block_residual(x1, w_norm, wq, wk, wv, wo, R[:1], eps=0.0, n_heads=8)
+    b, _ = orc.attention_block_residual(3.0 * x1, w_norm, wq, wk, wv, wo, R[:1], eps=0.0, n_heads=8)
+    np.testing.assert_allclose(b - 3.0 * x1, a - x1, rtol=1e-11, atol=1e-12)
+
+
+def test_residual_decode_equals_last_prefill_row():
+    x, wq, wk, wv, wo, R = tiny(seed=22, T=5)
+    w_norm = np.linspace(0.8, 1.2, x.shape[-1])
+    full, _ = orc.attention_block_residual(x, w_norm, wq, wk, wv, wo, R, n_heads=8)
+    ck = np.zeros((x.shape[0], 5, 2, 4))
+    cv = np.zeros_like(ck)
+    pre, ex = orc.attention_block_residual(x[:, :4], w_norm, wq, wk, wv, wo, R[:4], n_heads=8, cache_k=ck, cache_v=cv)
+    dec, _ = orc.attention_decode_residual(x[:, 4:], w_norm, wq, wk, wv, wo, R[4:5], ex["cache_k"], ex["cache_v"], 4, n_heads=8)
+    np.testing.assert_allclose(dec[:, 0], full[:, 4], rtol=1e-11, atol=1e-12)
+
+
+def test_planted_norm_mistakes_are_caught(monkeypatch):
+    c, eps = 0.003, 1e-5
+    w = np.linspace(0.5, 1.5, 64)
+    want = w * c / math.sqrt(c * c + eps)
+    good = orc.rms_norm
+
+    def no_eps(x, w, eps=orc.NORM_EPS):
+        x = np.asarray(x, dtype=np.float64)
+        return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) * w
+
+    def sum_not_mean(x, w, eps=orc.NORM_EPS):
+        x = np.asarray(x, dtype=np.float64)
+        return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps) * w
+
+    for bad in (no_eps, sum_not_mean):
+        monkeypatch.setattr(orc, "rms_norm", bad)
+        y = orc.rms_norm(np.full((1, 2, 64), c), w, eps)
+        assert not np.allclose(y, want, rtol=1e-6)
+    monkeypatch.setattr(orc, "rms_norm", good)
