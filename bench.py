@@ -35,6 +35,7 @@ from transformer_gqa_attention_gb300 import inputs as gin  # noqa: E402
 METRIC = "GQA block tokens/s & TFLOP/s (prefill), HBM GB/s (decode), % of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+NORM_EPS = 1e-5  # attention_norm epsilon of the residual workloads (norm_eps of the 8B configs)
 
 
 # ------------------------------------------------------------------ accounting
@@ -74,6 +75,8 @@ def kernel_work(kind, w: gin.Workload):
         return "hbm", float(6144 * 4096 * 2 + n_tok * 4096 * 2), "GB/s"
     if kind == "out_splitk":
         return "hbm", float(4096 * 4096 * 2 + n_tok * 4096 * 2), "GB/s"
+    if kind == "rms_norm":
+        return "hbm", float(n_tok * 4096 * 2 + n_tok * 4), "GB/s"
     return None, None, None
 
 
@@ -194,17 +197,24 @@ def oracle_sample_step(inp, w: gin.Workload, n_tokens: int, seqs: int, w64):
     from oracle import gqa_oracle as orc
     wq, wk, wv, wo = w64
     t0 = time.perf_counter()
+    wn = gin.to_f64(gin.norm_weight(w.seed)) if w.residual else None
     if w.kind == "prefill":
         x = gin.to_f64(inp.x[:seqs, :n_tokens])
         R = gin.to_f64(inp.R[:n_tokens])
-        orc.attention_block(x, wq, wk, wv, wo, R, causal=w.causal)
+        if w.residual:
+            orc.attention_block_residual(x, wn, wq, wk, wv, wo, R, causal=w.causal)
+        else:
+            orc.attention_block(x, wq, wk, wv, wo, R, causal=w.causal)
         units = seqs * n_tokens
     else:
         pos = w.start_pos
         x = gin.to_f64(inp.x[:seqs])
         ck = gin.to_f64(inp.cache_k[:seqs, :pos + 1])
         cv = gin.to_f64(inp.cache_v[:seqs, :pos + 1])
-        orc.attention_decode(x, wq, wk, wv, wo, gin.to_f64(inp.R), ck, cv, pos)
+        if w.residual:
+            orc.attention_decode_residual(x, wn, wq, wk, wv, wo, gin.to_f64(inp.R), ck, cv, pos)
+        else:
+            orc.attention_decode(x, wq, wk, wv, wo, gin.to_f64(inp.R), ck, cv, pos)
         units = seqs
     return time.perf_counter() - t0, units
 
@@ -286,6 +296,9 @@ def workload_config(w: gin.Workload):
     c = {"workload": w.name, "kind": w.kind, "B": w.B, "T": w.T, "start_pos": w.start_pos,
          "S_max": w.s_max, "causal": w.causal, "dim": 4096, "n_heads": 32, "n_kv_heads": 8,
          "head_dim": 128, "seed": w.seed, "l2": "flushed before every timed step (256 MiB write)"}
+    if w.residual:
+        c.update(residual=True, norm_eps=NORM_EPS,
+                 form="h = x + Delta_attn(attention_norm(x)); attention_norm weight 1 + 0.1 N(0,1)")
     return c
 
 
@@ -298,24 +311,34 @@ def run_gpu(args, w: gin.Workload, inp, world, rank, local):
     B, T = w.B, w.T
     S_max = w.s_max
     wts = [t.to(dev) for t in (inp.wq, inp.wk, inp.wv, inp.wo)]
-    ctx = abi.attn_create(*wts)
     stream = torch.cuda.current_stream(dev)
+    norm_w = gin.norm_weight(w.seed).to(dev) if w.residual else None
+
+    def new_ctx():
+        c = abi.attn_create(*wts)
+        if w.residual:
+            abi.attn_set_norm(c, norm_w, NORM_EPS, stream)
+        return c
+
+    ctx = new_ctx()
     x = inp.x.to(dev)
     R = inp.R.to(dev)
     if w.kind == "prefill":
         ck = torch.zeros(B, S_max, 8, 128, dtype=torch.bfloat16, device=dev)
         cv = torch.zeros_like(ck)
         delta = torch.empty(B, T, 4096, dtype=torch.float32, device=dev)
+        fn = abi.attn_prefill_residual if w.residual else abi.attn_prefill
 
         def step(xd=x, Rd=R, out=delta, c=ctx):
-            abi.attn_prefill(c, xd, B, T, Rd, w.causal, ck, cv, S_max, w.start_pos, out, stream)
+            fn(c, xd, B, T, Rd, w.causal, ck, cv, S_max, w.start_pos, out, stream)
     else:
         ck = inp.cache_k.to(dev)
         cv = inp.cache_v.to(dev)
         delta = torch.empty(B, 1, 4096, dtype=torch.float32, device=dev)
+        fn = abi.attn_decode_residual if w.residual else abi.attn_decode
 
         def step(xd=x, Rd=R, out=delta, c=ctx):
-            abi.attn_decode(c, xd, B, w.start_pos, Rd, ck, cv, S_max, out, stream)
+            fn(c, xd, B, w.start_pos, Rd, ck, cv, S_max, out, stream)
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
@@ -360,7 +383,7 @@ def run_gpu(args, w: gin.Workload, inp, world, rank, local):
     # Instead of an L2 flush (a device-timing artefact) consecutive steps alternate between
     # two contexts holding separate weight copies (2 x 84 MB > L2), so no step finds the
     # previous step's weights in L2.
-    ctx_alt = abi.attn_create(*wts)
+    ctx_alt = new_ctx()
     ctxs = (ctx, ctx_alt)
     x_h = inp.x.pin_memory()
     R_h = inp.R.pin_memory()

@@ -121,6 +121,55 @@ gqa_status attn_decode(gqa_ctx *ctx, const void *x, int B, int start_pos, const 
                        gqa_stream_t stream);
 
 /*
+ * The block's residual form.  The transformer block around this attention block computes
+ * h = x + Delta_attn(attention_norm(x)) (page "Llama 3.1 8B · Merge and project", code
+ * excerpt model.py 236-248 and "Contextual evidence from Output projection"), with
+ * attention_norm an RMSNorm of weight w and eps = norm_eps = 1e-05 (sku_list.py arch_args on
+ * the same page).  The pages do not print the RMSNorm body; it is read as
+ *     attention_norm(x)[t, j] = x[t, j] / sqrt(mean_k x[t, k]^2 + eps) * w[j].
+ * The library folds w into a second copy of W_Q, W_K, W_V (made by attn_set_norm) and scales
+ * each token row of the projections by 1 / rms in their epilogue; the residual add happens in
+ * the epilogue of the W_O projection.
+ */
+
+/*
+ * attn_set_norm — give the context the attention_norm weight.
+ *
+ * norm_w  [4096] bf16 device tensor, read during this call only (the folded copy it makes,
+ *         W_QKV * diag(norm_w) in bf16, 48 MiB, is owned by the context; a later call
+ *         replaces it).
+ * eps     the RMSNorm epsilon (> 0; 1e-5 for the Llama 3 / 3.1 8B configurations).
+ * Enqueued on `stream`.  Errors: GQA_ERR_INVALID_ARG (null, eps <= 0 or not finite),
+ * GQA_ERR_ALIGN, GQA_ERR_DEVICE, GQA_ERR_OOM, GQA_ERR_CUDA.
+ */
+gqa_status attn_set_norm(gqa_ctx *ctx, const void *norm_w, float eps, gqa_stream_t stream);
+
+/*
+ * attn_prefill_residual — h_out = x + Delta_attn(attention_norm(x)) for T new positions of
+ * B sequences: attn_prefill with the normalisation in front and the residual add behind.
+ *
+ * x       [B,T,4096] bf16: the residual stream entering the block (not normalised).
+ * h_out   [B,T,4096] fp32 output (x widened to fp32 plus Delta_attn), fully overwritten;
+ *         it must not overlap x.
+ * Every other argument, requirement and the cache semantics are those of attn_prefill.
+ * Errors: those of attn_prefill, and GQA_ERR_INVALID_ARG when attn_set_norm has not been
+ * called on the context.
+ */
+gqa_status attn_prefill_residual(gqa_ctx *ctx, const void *x, int B, int T, const float *R, int causal,
+                                 void *cache_k, void *cache_v, int S_max, int start_pos, float *h_out,
+                                 gqa_stream_t stream);
+
+/*
+ * attn_decode_residual — attn_decode in the residual form: x [B,1,4096] bf16 residual
+ * stream of the new token of each sequence, h_out [B,1,4096] fp32 = x + Delta_attn
+ * (must not overlap x).  Other arguments and errors as attn_decode, plus
+ * GQA_ERR_INVALID_ARG when attn_set_norm has not been called on the context.
+ */
+gqa_status attn_decode_residual(gqa_ctx *ctx, const void *x, int B, int start_pos, const float *R_row,
+                                void *cache_k, void *cache_v, int S_max, float *h_out,
+                                gqa_stream_t stream);
+
+/*
  * attn_sync_status — synchronise `stream`, then read and clear the context's device
  * status word.  Returns GQA_OK, GQA_ERR_TIMEOUT (a bounded device wait ran out in some
  * earlier call) or GQA_ERR_CUDA (the synchronisation itself failed).
@@ -148,7 +197,8 @@ enum {
     GQA_KERNEL_OUT_GEMM = 6,       /* Delta = H W_O^T (many tokens) */
     GQA_KERNEL_OUT_SPLITK = 7,     /* Delta = H W_O^T, few tokens: split-K partials */
     GQA_KERNEL_OUT_FINALIZE = 8,   /* split-K sum into Delta */
-    GQA_KERNEL_KINDS = 9
+    GQA_KERNEL_RMS_NORM = 9,       /* 1 / rms of each token row (residual form only) */
+    GQA_KERNEL_KINDS = 10
 };
 
 /*

@@ -113,3 +113,36 @@ def test_null_context_calls(L):
 def test_timeout_hook_validation(L):
     assert abi.raw_status("attn_debug_inject_timeout", None, 0) == 1
     assert abi.raw_status("attn_debug_inject_timeout", vp(FAKE), 99) == 1
+
+
+def residual_prefill_status(ctx=FAKE, x=FAKE, B=1, T=16, R=FAKE, ck=FAKE, cv=FAKE, S_max=16, start_pos=0,
+                            out=FAKE):
+    return abi.raw_status("attn_prefill_residual", vp(ctx) if ctx else None, vp(x) if x else None, B, T,
+                          vp(R) if R else None, 1, vp(ck) if ck else None, vp(cv) if cv else None, S_max,
+                          start_pos, vp(out) if out else None, None)
+
+
+def test_residual_entry_points_validate_before_use(L):
+    for kw in ("ctx", "x", "R", "ck", "cv", "out"):
+        assert residual_prefill_status(**{kw: 0}) == 1, kw
+    assert residual_prefill_status(T=0) == 2
+    assert residual_prefill_status(T=17, S_max=16) == 2
+    for kw in ("x", "R", "ck", "cv", "out"):
+        assert residual_prefill_status(**{kw: FAKE + 2}) == 3, kw
+    st = abi.raw_status("attn_decode_residual", vp(FAKE), vp(FAKE), 1025, 0, vp(FAKE), vp(FAKE), vp(FAKE), 16,
+                        vp(FAKE), None)
+    assert st == 2
+    st = abi.raw_status("attn_decode_residual", vp(FAKE), None, 1, 0, vp(FAKE), vp(FAKE), vp(FAKE), 16,
+                        vp(FAKE), None)
+    assert st == 1
+
+
+def test_set_norm_validation(L):
+    f = ctypes.c_float
+    assert abi.raw_status("attn_set_norm", None, vp(FAKE), f(1e-5), None) == 1
+    assert abi.raw_status("attn_set_norm", vp(FAKE), None, f(1e-5), None) == 1
+    assert abi.raw_status("attn_set_norm", vp(FAKE), vp(FAKE), f(0.0), None) == 1
+    assert abi.raw_status("attn_set_norm", vp(FAKE), vp(FAKE), f(-1.0), None) == 1
+    assert abi.raw_status("attn_set_norm", vp(FAKE), vp(FAKE), f(float("nan")), None) == 1
+    assert abi.raw_status("attn_set_norm", vp(FAKE), vp(FAKE), f(float("inf")), None) == 1
+    assert abi.raw_status("attn_set_norm", vp(FAKE), vp(FAKE + 2), f(1e-5), None) == 3

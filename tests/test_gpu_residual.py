@@ -1,0 +1,139 @@
+"""GPU parity of the block's residual form (attention_norm in front, residual add behind):
+attn_prefill_residual / attn_decode_residual against the fp64 oracle's
+attention_block_residual.  Both the output h = x + Delta and the update h - x are checked:
+x dominates h, so a check of h alone could hide an error in the update."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import gqa_oracle as orc
+from tests import gpu_util as gu
+from transformer_gqa_attention_gb300 import abi
+from transformer_gqa_attention_gb300 import inputs as gin
+
+pytestmark = pytest.mark.gpu
+
+EPS = 1e-5
+
+# The update h - x carries one bf16 rounding more than the block alone: attention_norm's weight
+# is folded into the projection weights, W diag(w) rounded to bf16 (the quoted model takes the
+# same extra rounding where it stores attention_norm(x) in bf16 before the projections).  On
+# top of the block's floor (~4.1e-3 rel-L1 from the bf16 Q_r, K_r, V, P and H) that rounding
+# adds ~1e-3; the bound keeps headroom for it.  h itself is held to the block's 5e-3.
+TOL_UPDATE_REL_L1 = 7e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from transformer_gqa_attention_gb300 import _build
+    _build.build()
+
+
+def _residual_block(inp, seed):
+    blk = gu.Block(inp)
+    wn = gin.norm_weight(seed)
+    abi.attn_set_norm(blk.ctx, wn.to(gu.DEV), EPS)
+    abi.attn_sync_status(blk.ctx)
+    return blk, gin.to_f64(wn)
+
+
+def _check(out, x, ref, what):
+    x64 = gin.to_f64(x)
+    gu.assert_close(gu.np64(out), ref, what=f"{what} h")
+    return gu.assert_close(gu.np64(out) - x64, ref - x64, TOL_UPDATE_REL_L1, gu.TOL_MAX, f"{what} update")
+
+
+@pytest.mark.parametrize("B,T", [(1, 16), (2, 3), (1, 129), (2, 300)])
+def test_prefill_residual_matches_oracle(B, T):
+    inp = gin.make_custom(seed=300 + T, B=B, T=T)
+    blk, wn = _residual_block(inp, 300 + T)
+    try:
+        x = inp.x.to(gu.DEV)
+        ck, cv = gu.empty_cache(B, T)
+        out = torch.empty(B, T, 4096, dtype=torch.float32, device=gu.DEV)
+        abi.attn_prefill_residual(blk.ctx, x, B, T, inp.R.to(gu.DEV), True, ck, cv, T, 0, out)
+        abi.attn_sync_status(blk.ctx)
+        wq, wk, wv, wo = blk.w64
+        ref, _ = orc.attention_block_residual(gin.to_f64(inp.x), wn, wq, wk, wv, wo, gin.to_f64(inp.R), eps=EPS)
+        _check(out, inp.x, ref, f"prefill B={B} T={T}")
+    finally:
+        blk.close()
+
+
+def test_prefill_residual_t2048_workload_sampled_rows():
+    inp = gin.make_inputs("prefill_b1_t2048_residual")
+    blk, wn = _residual_block(inp, inp.meta["seed"])
+    try:
+        B, T = inp.x.shape[:2]
+        ck, cv = gu.empty_cache(B, T)
+        out = torch.empty(B, T, 4096, dtype=torch.float32, device=gu.DEV)
+        abi.attn_prefill_residual(blk.ctx, inp.x.to(gu.DEV), B, T, inp.R.to(gu.DEV), True, ck, cv, T, 0, out)
+        abi.attn_sync_status(blk.ctx)
+        rows = gu.sample_rows(T)
+        wq, wk, wv, wo = blk.w64
+        ref, _ = orc.attention_block_residual(gin.to_f64(inp.x), wn, wq, wk, wv, wo, gin.to_f64(inp.R), eps=EPS,
+                                              rows=rows)
+        _check(out[:, rows], inp.x[:, rows], ref, "prefill T=2048 rows")
+    finally:
+        blk.close()
+
+
+def test_decode_residual_small_and_handoff():
+    B, T = 3, 40
+    inp = gin.make_custom(seed=310, B=B, T=T)
+    blk, wn = _residual_block(inp, 310)
+    try:
+        x = inp.x.to(gu.DEV)
+        R = inp.R.to(gu.DEV)
+        ck, cv = gu.empty_cache(B, T)
+        hp = torch.empty(B, T - 1, 4096, dtype=torch.float32, device=gu.DEV)
+        abi.attn_prefill_residual(blk.ctx, x[:, :T - 1].contiguous(), B, T - 1, R[:T - 1].contiguous(), True,
+                                  ck, cv, T, 0, hp)
+        hd = torch.empty(B, 1, 4096, dtype=torch.float32, device=gu.DEV)
+        abi.attn_decode_residual(blk.ctx, x[:, T - 1:].contiguous(), B, T - 1, R[T - 1:].contiguous(), ck, cv, T, hd)
+        abi.attn_sync_status(blk.ctx)
+        wq, wk, wv, wo = blk.w64
+        ref, _ = orc.attention_block_residual(gin.to_f64(inp.x), wn, wq, wk, wv, wo, gin.to_f64(inp.R), eps=EPS)
+        _check(hp, inp.x[:, :T - 1], ref[:, :T - 1], "prefill part")
+        _check(hd, inp.x[:, T - 1:], ref[:, T - 1:], "decode step")
+    finally:
+        blk.close()
+
+
+def test_decode_residual_b64_workload_sampled_sequences():
+    inp = gin.make_inputs("decode_b64_pos4095_residual")
+    pos = 4095
+    blk, wn = _residual_block(inp, inp.meta["seed"])
+    try:
+        ck = inp.cache_k.to(gu.DEV)
+        cv = inp.cache_v.to(gu.DEV)
+        out = torch.empty(64, 1, 4096, dtype=torch.float32, device=gu.DEV)
+        abi.attn_decode_residual(blk.ctx, inp.x.to(gu.DEV), 64, pos, inp.R.to(gu.DEV), ck, cv, 4096, out)
+        abi.attn_sync_status(blk.ctx)
+        wq, wk, wv, wo = blk.w64
+        for b in (0, 41, 63):
+            ref, _ = orc.attention_decode_residual(gin.to_f64(inp.x[b:b + 1]), wn, wq, wk, wv, wo, gin.to_f64(inp.R),
+                                                   gin.to_f64(inp.cache_k[b:b + 1]), gin.to_f64(inp.cache_v[b:b + 1]),
+                                                   pos, eps=EPS)
+            _check(out[b:b + 1], inp.x[b:b + 1], ref, f"decode seq {b}")
+    finally:
+        blk.close()
+
+
+def test_plain_block_unchanged_by_set_norm():
+    # attn_set_norm must not touch the plain path: attn_prefill gives the same bits before and after
+    B, T = 1, 200
+    inp = gin.make_custom(seed=320, B=B, T=T)
+    blk = gu.Block(inp)
+    try:
+        x = inp.x.to(gu.DEV)
+        R = inp.R.to(gu.DEV)
+        ck, cv = gu.empty_cache(B, T)
+        d0 = blk.prefill(x, R, ck, cv).clone()
+        abi.attn_set_norm(blk.ctx, gin.norm_weight(320).to(gu.DEV), EPS)
+        d1 = blk.prefill(x, R, ck, cv)
+        assert torch.equal(d0, d1)
+    finally:
+        blk.close()

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libgqa_attn.so")
 
-SOURCES = ["gqa_abi.cu", "gemm_launch.cu", "attn_launch.cu", "decode_noalloc.cu"]
+SOURCES = ["gqa_abi.cu", "gemm_launch.cu", "attn_launch.cu", "norm.cu", "decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

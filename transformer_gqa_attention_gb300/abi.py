@@ -17,14 +17,15 @@ STATUS_NAMES = {0: "GQA_OK", 1: "GQA_ERR_INVALID_ARG", 2: "GQA_ERR_SHAPE", 3: "G
                 4: "GQA_ERR_CUDA", 5: "GQA_ERR_TIMEOUT", 6: "GQA_ERR_OOM", 7: "GQA_ERR_DEVICE"}
 
 # Every symbol include/gqa_attn.h declares.
-EXPORTED = ("attn_create", "attn_prefill", "attn_decode", "attn_sync_status", "attn_debug_buffers",
+EXPORTED = ("attn_create", "attn_prefill", "attn_decode", "attn_set_norm", "attn_prefill_residual",
+            "attn_decode_residual", "attn_sync_status", "attn_debug_buffers",
             "attn_profile_begin", "attn_profile_end", "attn_debug_inject_timeout",
             "attn_decode_attention_noalloc",
             "attn_destroy", "attn_strerror", "attn_last_cuda_error")
 
 # Kernel kinds of attn_profile_end (GQA_KERNEL_* in include/gqa_attn.h).
 KERNEL_KINDS = ("qkv_gemm", "qkv_splitk", "qkv_finalize", "flash_prefill", "decode_attn",
-                "decode_combine", "out_gemm", "out_splitk", "out_finalize")
+                "decode_combine", "out_gemm", "out_splitk", "out_finalize", "rms_norm")
 
 _lib = None
 
@@ -55,6 +56,12 @@ def lib() -> ctypes.CDLL:
     L.attn_prefill.restype = i32
     L.attn_decode.argtypes = [vp, vp, i32, i32, vp, vp, vp, i32, vp, vp]
     L.attn_decode.restype = i32
+    L.attn_set_norm.argtypes = [vp, vp, ctypes.c_float, vp]
+    L.attn_set_norm.restype = i32
+    L.attn_prefill_residual.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp, i32, i32, vp, vp]
+    L.attn_prefill_residual.restype = i32
+    L.attn_decode_residual.argtypes = [vp, vp, i32, i32, vp, vp, vp, i32, vp, vp]
+    L.attn_decode_residual.restype = i32
     L.attn_sync_status.argtypes = [vp, vp]
     L.attn_sync_status.restype = i32
     L.attn_debug_buffers.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp)]
@@ -116,6 +123,22 @@ def attn_decode(ctx, x, B, start_pos, R_row, cache_k, cache_v, S_max, delta, str
     _check("attn_decode", lib().attn_decode(ctx, _ptr(x), int(B), int(start_pos), _ptr(R_row),
                                             _ptr(cache_k), _ptr(cache_v), int(S_max), _ptr(delta),
                                             _stream(stream)))
+
+
+def attn_set_norm(ctx, norm_w, eps=1e-5, stream=None):
+    _check("attn_set_norm", lib().attn_set_norm(ctx, _ptr(norm_w), float(eps), _stream(stream)))
+
+
+def attn_prefill_residual(ctx, x, B, T, R, causal, cache_k, cache_v, S_max, start_pos, h_out, stream=None):
+    _check("attn_prefill_residual",
+           lib().attn_prefill_residual(ctx, _ptr(x), int(B), int(T), _ptr(R), int(bool(causal)), _ptr(cache_k),
+                                       _ptr(cache_v), int(S_max), int(start_pos), _ptr(h_out), _stream(stream)))
+
+
+def attn_decode_residual(ctx, x, B, start_pos, R_row, cache_k, cache_v, S_max, h_out, stream=None):
+    _check("attn_decode_residual",
+           lib().attn_decode_residual(ctx, _ptr(x), int(B), int(start_pos), _ptr(R_row), _ptr(cache_k),
+                                      _ptr(cache_v), int(S_max), _ptr(h_out), _stream(stream)))
 
 
 def attn_sync_status(ctx, stream=None):

@@ -58,6 +58,7 @@ __device__ __forceinline__ void stage_chunk(float* stage, int lane, const uint32
 // 8k + lane/4 of the warp's 32 rows, columns 8 (lane & 3) .. +7 of the chunk.
 struct QkvRows {
   int m[4], b[4], t[4];
+  float rs[4];  // row scale (1 / rms of the token row under attention_norm; 1 for the block alone)
 };
 
 __device__ __forceinline__ QkvRows qkv_rows(const GemmParams& p, int lane, int m_base) {
@@ -68,6 +69,7 @@ __device__ __forceinline__ QkvRows qkv_rows(const GemmParams& p, int lane, int m
     const int mc = min(q.m[k], p.M - 1);
     q.b[k] = mc / p.T;
     q.t[k] = mc - q.b[k] * p.T;
+    q.rs[k] = p.row_scale ? __ldg(p.row_scale + mc) : 1.f;
   }
   return q;
 }
@@ -95,8 +97,11 @@ __device__ __forceinline__ void store_qkv_chunk(const GemmParams& p, const float
   for (int k = 0; k < 4; ++k) {
     const int r = 8 * k + (lane >> 2);
     if (q.m[k] >= p.M) continue;
-    const float4 x0 = *reinterpret_cast<const float4*>(stage + r * kEpiStride + 8 * cq);
-    const float4 x1 = *reinterpret_cast<const float4*>(stage + r * kEpiStride + 8 * cq + 4);
+    float4 x0 = *reinterpret_cast<const float4*>(stage + r * kEpiStride + 8 * cq);
+    float4 x1 = *reinterpret_cast<const float4*>(stage + r * kEpiStride + 8 * cq + 4);
+    const float rs = q.rs[k];
+    x0 = make_float4(x0.x * rs, x0.y * rs, x0.z * rs, x0.w * rs);
+    x1 = make_float4(x1.x * rs, x1.y * rs, x1.z * rs, x1.w * rs);
     uint4 w;
     if (is_v) {
       w = make_uint4(pack_bf16x2(x0.x, x0.y), pack_bf16x2(x0.z, x0.w), pack_bf16x2(x1.x, x1.y),
@@ -119,17 +124,37 @@ __device__ __forceinline__ void store_qkv_chunk(const GemmParams& p, const float
   }
 }
 
+// four bf16 (8 bytes) widened to fp32
+__device__ __forceinline__ float4 bf16x4_to_float4(uint2 v) {
+  return make_float4(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x), bf16lo_to_f32(v.y), bf16hi_to_f32(v.y));
+}
+
 // fp32 epilogue of one staged chunk: 8 passes of 4 rows, lane -> row 4k + lane/8, columns
-// col0 + 4 (lane & 7) .. +3.
+// col0 + 4 (lane & 7) .. +3; with a residual, its bf16 values are read (all passes before
+// the first store) and added.
 __device__ __forceinline__ void store_f32_chunk(const GemmParams& p, const float* stage, int lane, int m_base,
                                                 int col0) {
+  const int c4 = col0 + 4 * (lane & 7);
+  uint2 rv[8];
+  if (p.residual) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int m = min(m_base + 4 * k + (lane >> 3), p.M - 1);
+      rv[k] = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.residual) +
+                                                   static_cast<size_t>(m) * 4096 + c4));
+    }
+  }
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const int r = 4 * k + (lane >> 3);
     const int m = m_base + r;
     if (m >= p.M) continue;
-    const float4 x = *reinterpret_cast<const float4*>(stage + r * kEpiStride + 4 * (lane & 7));
-    *reinterpret_cast<float4*>(static_cast<float*>(p.out0) + static_cast<size_t>(m) * p.ldo + col0 + 4 * (lane & 7)) = x;
+    float4 x = *reinterpret_cast<const float4*>(stage + r * kEpiStride + 4 * (lane & 7));
+    if (p.residual) {
+      const float4 h = bf16x4_to_float4(rv[k]);
+      x = make_float4(h.x + x.x, h.y + x.y, h.z + x.z, h.w + x.w);
+    }
+    *reinterpret_cast<float4*>(static_cast<float*>(p.out0) + static_cast<size_t>(m) * p.ldo + c4) = x;
   }
 }
 
@@ -560,8 +585,17 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       if constexpr (EPI == kSplitKOut) {
+        if (p.residual) {  // x + Delta
+          const float4 h = bf16x4_to_float4(__ldg(reinterpret_cast<const uint2*>(
+              static_cast<const __nv_bfloat16*>(p.residual) + static_cast<size_t>(tok) * 4096 + m)));
+          acc = make_float4(h.x + acc.x, h.y + acc.y, h.z + acc.z, h.w + acc.w);
+        }
         *reinterpret_cast<float4*>(static_cast<float*>(p.fin0) + static_cast<size_t>(tok) * 4096 + m) = acc;
       } else {
+        if (p.row_scale) {  // attention_norm: the token row's 1 / rms
+          const float rs = __ldg(p.row_scale + tok);
+          acc = make_float4(acc.x * rs, acc.y * rs, acc.z * rs, acc.w * rs);
+        }
         const int b = tok / p.T;
         const int t = tok - b * p.T;
         if (rope) {

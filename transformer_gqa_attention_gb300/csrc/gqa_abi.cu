@@ -25,6 +25,9 @@ struct gqa_ctx {
   // weights, k-block-major: W_t[kb][row][64] for kb = 0..63
   __nv_bfloat16* w_qkv = nullptr;  // 6144 rows: W_Q rows 0..4095, W_K 4096..5119, W_V 5120..6143
   __nv_bfloat16* w_o = nullptr;    // 4096 rows
+  // residual form: W_QKV * diag(attention_norm weight), same layout (attn_set_norm)
+  __nv_bfloat16* w_qkv_norm = nullptr;
+  float norm_eps = 0.f;
   int* status = nullptr;           // device status word (kDevErr* bits)
   int* counters = nullptr;         // arrival counters of the decode split merge (kCounterInts)
   uint8_t* ws = nullptr;           // workspace
@@ -144,7 +147,7 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // ------------------------------------------------------------------ workspace
 struct WsLayout {
-  size_t q_off, h_off, dec_o_off, dec_ml_off, total;
+  size_t q_off, h_off, dec_o_off, dec_ml_off, rstd_off, total;
 };
 
 struct SkinnyPlan {
@@ -195,6 +198,8 @@ WsLayout ws_layout(long long n_tok, const SkinnyPlan* sk, const DecodePlan* dp, 
     w.dec_ml_off = off;
     off = round_up(off + units * 4 * 2 * 4, 256);
   }
+  w.rstd_off = off;  // residual form: 1 / rms per token row
+  off = round_up(off + static_cast<size_t>(n_tok) * 4, 256);
   w.total = off;
   return w;
 }
@@ -263,8 +268,11 @@ const float kScaleLog2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0
 // Q/K/V projection + RoPE + cache write for n_tok tokens laid out [B, T] (steps 1-5).
 gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, void* ck, void* cv,
                    int S_max, int start_pos, void* q_out, const WsLayout& w, const SkinnyPlan* sk,
-                   cudaStream_t s) {
+                   const float* row_scale, cudaStream_t s) {
   GemmParams p{};
+  // residual form: the folded weights, each token row scaled by its 1 / rms
+  const __nv_bfloat16* wqkv = row_scale ? c->w_qkv_norm : c->w_qkv;
+  p.row_scale = row_scale;
   p.T = T;
   p.S_max = S_max;
   p.start_pos = start_pos;
@@ -272,7 +280,7 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
   p.num_kb = 64;
   CUtensorMap ta, tb;
   if (sk) {
-    if (!map_weight_tiled(&ta, c->w_qkv, 6144, 128) || !map_rows_k4096(&tb, x, n_tok, 64))
+    if (!map_weight_tiled(&ta, wqkv, 6144, 128) || !map_rows_k4096(&tb, x, n_tok, 64))
       return cuda_fail(cudaErrorInvalidValue);
     p.M = 6144;
     p.N = n_tok;
@@ -289,7 +297,7 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
     { ProfScope ps(c, GQA_KERNEL_QKV_SPLITK, s); GQA_CUDA(launch_gemm_splitk_qkv(ta, tb, p, grid, s)); }
   } else {
     // CTA pairs, 256x256 tiles: each CTA loads 128-row boxes of x and of W_QKV
-    if (!map_rows_k4096(&ta, x, n_tok, 128) || !map_weight_tiled(&tb, c->w_qkv, 6144, 128))
+    if (!map_rows_k4096(&ta, x, n_tok, 128) || !map_weight_tiled(&tb, wqkv, 6144, 128))
       return cuda_fail(cudaErrorInvalidValue);
     p.M = n_tok;
     p.N = 6144;
@@ -310,8 +318,9 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
 
 // Delta = H W_O^T (step 14).
 gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsLayout& w,
-                   const SkinnyPlan* sk, cudaStream_t s) {
+                   const SkinnyPlan* sk, const void* residual, cudaStream_t s) {
   GemmParams p{};
+  p.residual = residual;  // residual form: x + Delta
   p.status = c->status;
   p.num_kb = 64;
   CUtensorMap ta, tb;
@@ -409,17 +418,30 @@ gqa_status attn_create(const void* wq, const void* wk, const void* wv, const voi
   return GQA_OK;
 }
 
-gqa_status attn_prefill(gqa_ctx* c, const void* x, int B, int T, const float* R, int causal, void* cache_k,
-                        void* cache_v, int S_max, int start_pos, float* delta, gqa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// 1 / rms of each of the n_tok token rows of x (residual form), into the workspace.
+gqa_status run_rms(gqa_ctx* c, const void* x, int n_tok, const WsLayout& w, cudaStream_t s) {
+  float* r = reinterpret_cast<float*>(c->ws + w.rstd_off);
+  { ProfScope ps(c, GQA_KERNEL_RMS_NORM, s); GQA_CUDA(launch_rms_rstd(x, n_tok, c->norm_eps, r, s)); }
+  return GQA_OK;
+}
+
+// The block (residual == false: out = Delta of x) or its residual form (out = x +
+// Delta(attention_norm(x))).
+gqa_status prefill_impl(gqa_ctx* c, const void* x, int B, int T, const float* R, int causal, void* cache_k,
+                        void* cache_v, int S_max, int start_pos, float* delta, bool residual, cudaStream_t s) {
   if (!c || !x || !R || !cache_k || !cache_v || !delta) return GQA_ERR_INVALID_ARG;
   if (B < 1 || T < 1 || start_pos < 0 || S_max < 1 || S_max > kMaxSMax) return GQA_ERR_SHAPE;
   if (static_cast<long long>(start_pos) + T > S_max) return GQA_ERR_SHAPE;
   if (static_cast<long long>(B) * T > kMaxTokens) return GQA_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(R) || !aligned16(cache_k) || !aligned16(cache_v) || !aligned16(delta))
     return GQA_ERR_ALIGN;
+  if (residual && !c->w_qkv_norm) return GQA_ERR_INVALID_ARG;  // attn_set_norm not called
   gqa_status st = check_device(c);
   if (st != GQA_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   const int n_tok = B * T;
   SkinnyPlan sk_v = skinny_plan(n_tok, c->num_sms);
@@ -432,7 +454,12 @@ gqa_status attn_prefill(gqa_ctx* c, const void* x, int B, int T, const float* R,
   c->last_q = q_r;
   c->last_h = h;
 
-  st = run_qkv(c, x, n_tok, T, R, cache_k, cache_v, S_max, start_pos, q_r, w, sk, s);
+  const float* row_scale = nullptr;
+  if (residual) {
+    if ((st = run_rms(c, x, n_tok, w, s)) != GQA_OK) return st;
+    row_scale = reinterpret_cast<const float*>(c->ws + w.rstd_off);
+  }
+  st = run_qkv(c, x, n_tok, T, R, cache_k, cache_v, S_max, start_pos, q_r, w, sk, row_scale, s);
   if (st != GQA_OK) return st;
 
   // steps 6-13: causal GQA flash attention over keys 0 .. start_pos+T-1
@@ -473,19 +500,19 @@ gqa_status attn_prefill(gqa_ctx* c, const void* x, int B, int T, const float* R,
   }
   { ProfScope ps(c, GQA_KERNEL_FLASH_PREFILL, s); GQA_CUDA(launch_flash_prefill(tq, tk, tv, th, fp, dim3(B * 16 * fp.n_qtiles), s)); }
 
-  return run_out(c, h, n_tok, delta, w, sk, s);
+  return run_out(c, h, n_tok, delta, w, sk, residual ? x : nullptr, s);
 }
 
-gqa_status attn_decode(gqa_ctx* c, const void* x, int B, int start_pos, const float* R_row, void* cache_k,
-                       void* cache_v, int S_max, float* delta, gqa_stream_t stream) {
+gqa_status decode_impl(gqa_ctx* c, const void* x, int B, int start_pos, const float* R_row, void* cache_k,
+                       void* cache_v, int S_max, float* delta, bool residual, cudaStream_t s) {
   if (!c || !x || !R_row || !cache_k || !cache_v || !delta) return GQA_ERR_INVALID_ARG;
   if (B < 1 || B > kDecodeMaxBatch || start_pos < 0 || S_max < 1 || S_max > kMaxSMax || start_pos >= S_max)
     return GQA_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(R_row) || !aligned16(cache_k) || !aligned16(cache_v) || !aligned16(delta))
     return GQA_ERR_ALIGN;
+  if (residual && !c->w_qkv_norm) return GQA_ERR_INVALID_ARG;  // attn_set_norm not called
   gqa_status st = check_device(c);
   if (st != GQA_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   const int kv_len = start_pos + 1;
   SkinnyPlan sk_v = skinny_plan(B, c->num_sms);
@@ -500,7 +527,12 @@ gqa_status attn_decode(gqa_ctx* c, const void* x, int B, int start_pos, const fl
   c->last_h = h;
 
   // steps 1-5 for the new token of each sequence (T = 1, position start_pos)
-  st = run_qkv(c, x, B, 1, R_row, cache_k, cache_v, S_max, start_pos, q_r, w, sk, s);
+  const float* row_scale = nullptr;
+  if (residual) {
+    if ((st = run_rms(c, x, B, w, s)) != GQA_OK) return st;
+    row_scale = reinterpret_cast<const float*>(c->ws + w.rstd_off);
+  }
+  st = run_qkv(c, x, B, 1, R_row, cache_k, cache_v, S_max, start_pos, q_r, w, sk, row_scale, s);
   if (st != GQA_OK) return st;
 
   // steps 6-13 against the cache (no mask: every key 0..start_pos is visible)
@@ -524,7 +556,52 @@ gqa_status attn_decode(gqa_ctx* c, const void* x, int B, int start_pos, const fl
   { ProfScope ps(c, GQA_KERNEL_DECODE_ATTN, s); GQA_CUDA(launch_decode_attn(tk, tv, p, dim3(dp.n_splits, 8, B), s)); }
 
   // step 14
-  return run_out(c, h, B, delta, w, sk, s);
+  return run_out(c, h, B, delta, w, sk, residual ? x : nullptr, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+gqa_status attn_prefill(gqa_ctx* c, const void* x, int B, int T, const float* R, int causal, void* cache_k,
+                        void* cache_v, int S_max, int start_pos, float* delta, gqa_stream_t stream) {
+  return prefill_impl(c, x, B, T, R, causal, cache_k, cache_v, S_max, start_pos, delta, false,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+gqa_status attn_prefill_residual(gqa_ctx* c, const void* x, int B, int T, const float* R, int causal,
+                                 void* cache_k, void* cache_v, int S_max, int start_pos, float* h_out,
+                                 gqa_stream_t stream) {
+  return prefill_impl(c, x, B, T, R, causal, cache_k, cache_v, S_max, start_pos, h_out, true,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+gqa_status attn_decode(gqa_ctx* c, const void* x, int B, int start_pos, const float* R_row, void* cache_k,
+                       void* cache_v, int S_max, float* delta, gqa_stream_t stream) {
+  return decode_impl(c, x, B, start_pos, R_row, cache_k, cache_v, S_max, delta, false,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+gqa_status attn_decode_residual(gqa_ctx* c, const void* x, int B, int start_pos, const float* R_row,
+                                void* cache_k, void* cache_v, int S_max, float* h_out, gqa_stream_t stream) {
+  return decode_impl(c, x, B, start_pos, R_row, cache_k, cache_v, S_max, h_out, true,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+gqa_status attn_set_norm(gqa_ctx* c, const void* norm_w, float eps, gqa_stream_t stream) {
+  if (!c || !norm_w || !(eps > 0.f) || !std::isfinite(eps)) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(norm_w)) return GQA_ERR_ALIGN;
+  gqa_status st = check_device(c);
+  if (st != GQA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!c->w_qkv_norm && cudaMalloc(&c->w_qkv_norm, size_t(6144) * 4096 * 2) != cudaSuccess) {
+    cudaGetLastError();
+    c->w_qkv_norm = nullptr;
+    return GQA_ERR_OOM;
+  }
+  GQA_CUDA(launch_fold_norm_weight(c->w_qkv, norm_w, 6144, c->w_qkv_norm, s));
+  c->norm_eps = eps;
+  return GQA_OK;
 }
 
 gqa_status attn_sync_status(gqa_ctx* c, gqa_stream_t stream) {
@@ -601,6 +678,7 @@ void attn_destroy(gqa_ctx* c) {
   for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
   if (c->w_qkv) cudaFree(c->w_qkv);
   if (c->w_o) cudaFree(c->w_o);
+  if (c->w_qkv_norm) cudaFree(c->w_qkv_norm);
   if (c->status) cudaFree(c->status);
   if (c->counters) cudaFree(c->counters);
   if (c->ws) cudaFree(c->ws);

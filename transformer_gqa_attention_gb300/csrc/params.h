@@ -36,6 +36,9 @@ struct GemmParams {
   void* fin2;        // kSplitKQkv: cache_v
   int* status;
   int fault;         // test hook: the first work unit's producer issues no loads (its waits run out)
+  // residual form of the block (both null for the block alone)
+  const float* row_scale;  // Q/K/V epilogues: 1 / rms of each token row (attention_norm)
+  const void* residual;    // Delta epilogues: x [tokens, 4096] bf16, added to Delta
 };
 
 struct FlashParams {

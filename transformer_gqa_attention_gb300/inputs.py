@@ -44,6 +44,7 @@ class Workload:
     causal: bool = True
     start_pos: int = 0
     S_max: int = 0  # 0 -> start_pos + T
+    residual: bool = False  # attention_norm in front and the residual add behind
 
     @property
     def s_max(self) -> int:
@@ -54,7 +55,8 @@ class Workload:
         return self.B * self.T
 
 
-# The five workloads the block is measured and checked on.
+# The workloads the block is measured and checked on: the five shapes of the block itself,
+# then two of them through the residual form.
 WORKLOADS = {
     w.name: w
     for w in [
@@ -63,6 +65,11 @@ WORKLOADS = {
         Workload("prefill_b4_t8192", "prefill", B=4, T=8192, seed=2),
         Workload("decode_b64_pos4095", "decode", B=64, T=1, seed=3, start_pos=4095, S_max=4096),
         Workload("prefill_b1_t32768", "prefill", B=1, T=32768, seed=4),
+        # the same shapes through the block's residual form (attention_norm in front, the
+        # residual add behind); x is then the residual stream
+        Workload("prefill_b1_t2048_residual", "prefill", B=1, T=2048, seed=1, residual=True),
+        Workload("decode_b64_pos4095_residual", "decode", B=64, T=1, seed=3, start_pos=4095, S_max=4096,
+                 residual=True),
     ]
 }
 
@@ -147,6 +154,16 @@ def make_custom(seed: int, B: int, T: int, *, start_pos: int = 0, S_max: int | N
                        meta=dict(name=f"custom_s{seed}_b{B}_t{T}_p{start_pos}", kind="prefill",
                                  B=B, T=T, seed=seed, causal=True, start_pos=start_pos,
                                  S_max=s_max))
+
+
+NORM_W_STD = 0.1
+
+
+def norm_weight(seed: int, dim: int = DIM) -> torch.Tensor:
+    """attention_norm weight [dim] bf16 = 1 + 0.1 N(0, 1), from its own generator (seeded
+    from the workload seed) so that the block's inputs keep their draw order."""
+    gen = torch.Generator("cpu").manual_seed(seed + (1 << 20))
+    return (1.0 + torch.randn(dim, generator=gen, dtype=torch.float32) * NORM_W_STD).to(torch.bfloat16)
 
 
 def to_f64(t: torch.Tensor) -> np.ndarray:
