@@ -155,6 +155,59 @@ def test_decode_equals_last_prefill_row_on_gpu():
         blk.close()
 
 
+def test_prefill_maximum_token_count():
+    # B*T at the documented limit (262144): GEMM M = 262144, 32768 attention CTAs, a 4 GB
+    # workspace; a few sequences checked against the oracle
+    B, T = 2048, 128
+    inp = gin.make_custom(seed=71, B=B, T=T)
+    blk = gu.Block(inp)
+    try:
+        ck, cv = gu.empty_cache(B, T)
+        delta = blk.prefill(inp.x.to(gu.DEV), inp.R.to(gu.DEV), ck, cv)
+        wq, wk, wv, wo = blk.w64
+        for b in (0, 1023, 2047):
+            ref, _ = orc.attention_block(gin.to_f64(inp.x[b:b + 1]), wq, wk, wv, wo, gin.to_f64(inp.R))
+            gu.assert_close(gu.np64(delta[b:b + 1]), ref, what=f"max-token prefill seq {b}")
+    finally:
+        blk.close()
+
+
+def test_decode_maximum_s_max():
+    # S_max at the documented limit (2^20 positions per sequence, 2 GB between sequences);
+    # positions past the 131072 seeded keys hold NaN, so any read beyond kv_len shows
+    B, S_max, pos = 2, 1 << 20, 131071
+    inp = gin.make_custom(seed=72, B=B, T=1, start_pos=pos, S_max=pos + 1, fill_cache=True)
+    blk = gu.Block(inp)
+    try:
+        ck, cv = gu.empty_cache(B, S_max)
+        ck[:, :pos + 1] = inp.cache_k.to(gu.DEV)
+        cv[:, :pos + 1] = inp.cache_v.to(gu.DEV)
+        delta = blk.decode(inp.x.to(gu.DEV), inp.R.to(gu.DEV), ck, cv, pos)
+        assert torch.isnan(ck[:, pos + 1:pos + 65].float()).all()  # nothing written past the slot
+        wq, wk, wv, wo = blk.w64
+        ref, _ = orc.attention_decode(gin.to_f64(inp.x), wq, wk, wv, wo, gin.to_f64(inp.R),
+                                      gin.to_f64(inp.cache_k), gin.to_f64(inp.cache_v), pos)
+        gu.assert_close(gu.np64(delta), ref, what="decode at S_max = 2^20")
+    finally:
+        blk.close()
+
+
+def test_decode_maximum_batch():
+    # B at the decode limit (1024): the projections take the many-token path
+    B, pos = 1024, 199
+    inp = gin.make_custom(seed=73, B=B, T=1, start_pos=pos, S_max=pos + 1, fill_cache=True)
+    blk = gu.Block(inp)
+    try:
+        delta = blk.decode(inp.x.to(gu.DEV), inp.R.to(gu.DEV), inp.cache_k.to(gu.DEV), inp.cache_v.to(gu.DEV), pos)
+        wq, wk, wv, wo = blk.w64
+        for b in (0, 511, 1023):
+            ref, _ = orc.attention_decode(gin.to_f64(inp.x[b:b + 1]), wq, wk, wv, wo, gin.to_f64(inp.R),
+                                          gin.to_f64(inp.cache_k[b:b + 1]), gin.to_f64(inp.cache_v[b:b + 1]), pos)
+            gu.assert_close(gu.np64(delta[b:b + 1]), ref, what=f"max-batch decode seq {b}")
+    finally:
+        blk.close()
+
+
 def test_causality_and_determinism_bit_exact():
     B, T, t0 = 1, 300, 130
     inp = gin.make_custom(seed=51, B=B, T=T)
