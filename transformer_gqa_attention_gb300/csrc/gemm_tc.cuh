@@ -325,26 +325,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     int lt = 0;
     for (int u = pair; u < total_units; u += n_pairs, ++lt) {
       const int ab = lt & 1;
+      const int m_base = (u / p.n_tiles) * 256 + 128 * rank + quarter * 32;
+      const int n0 = (u % p.n_tiles) * 256;
+      // Q/K tiles: all rotation coefficients of the tile are read before waiting for the
+      // accumulator, so their latency hides under the main loop (chunks cp and cp + 4, the
+      // tile's two 128-column head slices, share RoPE pairs)
+      const bool rope = EPI == kQkvRope && n0 < 5120;
+      QkvRows qr{};
+      float4 cs[4][4][2];
+      if constexpr (EPI == kQkvRope) {
+        qr = qkv_rows(p, lane, m_base);
+        if (rope) {
+#pragma unroll
+          for (int cp = 0; cp < 4; ++cp) load_rope(p, qr, lane, cp, cs[cp]);
+        }
+      }
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[ab], (lt >> 1) & 1, abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + lane_off + ab * 256;
-      const int m_base = (u / p.n_tiles) * 256 + 128 * rank + quarter * 32;
-      const int n0 = (u % p.n_tiles) * 256;
-      // chunks cp and cp + 4 (the tile's two 128-column head slices) share RoPE pairs; the
-      // next pair's table reads are issued before this pair is stored
-      const bool rope = EPI == kQkvRope && n0 < 5120;
-      QkvRows qr{};
-      float4 cs[4][2], cs_next[4][2];
-      if constexpr (EPI == kQkvRope) {
-        qr = qkv_rows(p, lane, m_base);
-        if (rope) load_rope(p, qr, lane, 0, cs);
-      }
-#pragma unroll 1
+#pragma unroll
       for (int cp = 0; cp < 4; ++cp) {
-        if constexpr (EPI == kQkvRope) {
-          if (rope && cp < 3) load_rope(p, qr, lane, cp + 1, cs_next);
-        }
         uint32_t va[32], vb[32];
         tmem_ld32(t_row + cp * 32, va);
         tmem_ld32(t_row + (cp + 4) * 32, vb);
@@ -352,7 +353,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         stage_chunk(stage, lane, va);
         __syncwarp();
         if constexpr (EPI == kQkvRope) {
-          store_qkv_chunk(p, stage, lane, qr, n0 + cp * 32, cs);
+          store_qkv_chunk(p, stage, lane, qr, n0 + cp * 32, cs[cp]);
         } else {
           store_f32_chunk(p, stage, lane, m_base, n0 + cp * 32);
         }
@@ -360,20 +361,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         stage_chunk(stage, lane, vb);
         __syncwarp();
         if constexpr (EPI == kQkvRope) {
-          store_qkv_chunk(p, stage, lane, qr, n0 + (cp + 4) * 32, cs);
+          store_qkv_chunk(p, stage, lane, qr, n0 + (cp + 4) * 32, cs[cp]);
         } else {
           store_f32_chunk(p, stage, lane, m_base, n0 + (cp + 4) * 32);
         }
         __syncwarp();
-        if constexpr (EPI == kQkvRope) {
-          if (rope && cp < 3) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              cs[k][0] = cs_next[k][0];
-              cs[k][1] = cs_next[k][1];
-            }
-          }
-        }
       }
       tc_fence_before();
       __syncwarp();
