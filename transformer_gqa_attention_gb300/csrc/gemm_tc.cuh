@@ -129,21 +129,24 @@ __device__ __forceinline__ float4 bf16x4_to_float4(uint2 v) {
   return make_float4(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x), bf16lo_to_f32(v.y), bf16hi_to_f32(v.y));
 }
 
-// fp32 epilogue of one staged chunk: 8 passes of 4 rows, lane -> row 4k + lane/8, columns
-// col0 + 4 (lane & 7) .. +3; with a residual, its bf16 values are read (all passes before
-// the first store) and added.
-__device__ __forceinline__ void store_f32_chunk(const GemmParams& p, const float* stage, int lane, int m_base,
-                                                int col0) {
+// Residual values (bf16, 4 per lane and pass) a lane adds in store_f32_chunk for the chunk at
+// columns col0 .. col0+31.
+__device__ __forceinline__ void load_residual_chunk(const GemmParams& p, int lane, int m_base, int col0,
+                                                    uint2 (&rv)[8]) {
   const int c4 = col0 + 4 * (lane & 7);
-  uint2 rv[8];
-  if (p.residual) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int m = min(m_base + 4 * k + (lane >> 3), p.M - 1);
-      rv[k] = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.residual) +
-                                                   static_cast<size_t>(m) * 4096 + c4));
-    }
+  for (int k = 0; k < 8; ++k) {
+    const int m = min(m_base + 4 * k + (lane >> 3), p.M - 1);
+    rv[k] = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.residual) +
+                                                 static_cast<size_t>(m) * 4096 + c4));
   }
+}
+
+// fp32 epilogue of one staged chunk: 8 passes of 4 rows, lane -> row 4k + lane/8, columns
+// col0 + 4 (lane & 7) .. +3; with a residual, the values read by load_residual_chunk are added.
+__device__ __forceinline__ void store_f32_chunk(const GemmParams& p, const float* stage, int lane, int m_base,
+                                                int col0, const uint2 (&rv)[8]) {
+  const int c4 = col0 + 4 * (lane & 7);
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const int r = 4 * k + (lane >> 3);
@@ -333,11 +336,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       const bool rope = EPI == kQkvRope && n0 < 5120;
       QkvRows qr{};
       float4 cs[4][4][2];
+      // Delta tiles with a residual: the residual of chunk pair cp + 1 is read while pair cp
+      // is stored (pair 0 before the accumulator wait)
+      uint2 rva[8], rvb[8], rva_n[8], rvb_n[8];
       if constexpr (EPI == kQkvRope) {
         qr = qkv_rows(p, lane, m_base);
         if (rope) {
 #pragma unroll
           for (int cp = 0; cp < 4; ++cp) load_rope(p, qr, lane, cp, cs[cp]);
+        }
+      } else {
+        if (p.residual) {
+          load_residual_chunk(p, lane, m_base, n0, rva);
+          load_residual_chunk(p, lane, m_base, n0 + 128, rvb);
         }
       }
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[ab], (lt >> 1) & 1, abort_flag, p.status));
@@ -346,6 +357,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       const uint32_t t_row = tmem_base + lane_off + ab * 256;
 #pragma unroll
       for (int cp = 0; cp < 4; ++cp) {
+        if constexpr (EPI == kStoreF32) {
+          if (p.residual && cp < 3) {
+            load_residual_chunk(p, lane, m_base, n0 + (cp + 1) * 32, rva_n);
+            load_residual_chunk(p, lane, m_base, n0 + (cp + 5) * 32, rvb_n);
+          }
+        }
         uint32_t va[32], vb[32];
         tmem_ld32(t_row + cp * 32, va);
         tmem_ld32(t_row + (cp + 4) * 32, vb);
@@ -355,7 +372,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         if constexpr (EPI == kQkvRope) {
           store_qkv_chunk(p, stage, lane, qr, n0 + cp * 32, cs[cp]);
         } else {
-          store_f32_chunk(p, stage, lane, m_base, n0 + cp * 32);
+          store_f32_chunk(p, stage, lane, m_base, n0 + cp * 32, rva);
         }
         __syncwarp();
         stage_chunk(stage, lane, vb);
@@ -363,9 +380,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         if constexpr (EPI == kQkvRope) {
           store_qkv_chunk(p, stage, lane, qr, n0 + (cp + 4) * 32, cs[cp]);
         } else {
-          store_f32_chunk(p, stage, lane, m_base, n0 + (cp + 4) * 32);
+          store_f32_chunk(p, stage, lane, m_base, n0 + (cp + 4) * 32, rvb);
         }
         __syncwarp();
+        if constexpr (EPI == kStoreF32) {
+          if (p.residual && cp < 3) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              rva[k] = rva_n[k];
+              rvb[k] = rvb_n[k];
+            }
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
