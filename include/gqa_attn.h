@@ -189,16 +189,13 @@ gqa_status attn_debug_buffers(gqa_ctx *ctx, const void **q_r, const void **h);
  */
 enum {
     GQA_KERNEL_QKV_GEMM = 0,       /* fused Q/K/V projection + RoPE + cache write (many tokens) */
-    GQA_KERNEL_QKV_SPLITK = 1,     /* Q/K/V projection, few tokens: split-K partials */
-    GQA_KERNEL_QKV_FINALIZE = 2,   /* split-K sum + RoPE + cache write */
-    GQA_KERNEL_FLASH_PREFILL = 3,  /* causal GQA attention, prefill */
-    GQA_KERNEL_DECODE_ATTN = 4,    /* split-KV attention, decode */
-    GQA_KERNEL_DECODE_COMBINE = 5, /* merge of the key splits */
-    GQA_KERNEL_OUT_GEMM = 6,       /* Delta = H W_O^T (many tokens) */
-    GQA_KERNEL_OUT_SPLITK = 7,     /* Delta = H W_O^T, few tokens: split-K partials */
-    GQA_KERNEL_OUT_FINALIZE = 8,   /* split-K sum into Delta */
-    GQA_KERNEL_RMS_NORM = 9,       /* 1 / rms of each token row (residual form only) */
-    GQA_KERNEL_KINDS = 10
+    GQA_KERNEL_QKV_SPLITK = 1,     /* the same for few tokens: cluster split-K with its reduction */
+    GQA_KERNEL_FLASH_PREFILL = 2,  /* causal GQA attention, prefill */
+    GQA_KERNEL_DECODE_ATTN = 3,    /* split-KV attention with the fused merge, decode */
+    GQA_KERNEL_OUT_GEMM = 4,       /* Delta = H W_O^T (many tokens) */
+    GQA_KERNEL_OUT_SPLITK = 5,     /* the same for few tokens */
+    GQA_KERNEL_RMS_NORM = 6,       /* 1 / rms of each token row (residual form only) */
+    GQA_KERNEL_KINDS = 7
 };
 
 /*

@@ -24,8 +24,8 @@ EXPORTED = ("attn_create", "attn_prefill", "attn_decode", "attn_set_norm", "attn
             "attn_destroy", "attn_strerror", "attn_last_cuda_error")
 
 # Kernel kinds of attn_profile_end (GQA_KERNEL_* in include/gqa_attn.h).
-KERNEL_KINDS = ("qkv_gemm", "qkv_splitk", "qkv_finalize", "flash_prefill", "decode_attn",
-                "decode_combine", "out_gemm", "out_splitk", "out_finalize", "rms_norm")
+KERNEL_KINDS = ("qkv_gemm", "qkv_splitk", "flash_prefill", "decode_attn", "out_gemm", "out_splitk",
+                "rms_norm")
 
 _lib = None
 

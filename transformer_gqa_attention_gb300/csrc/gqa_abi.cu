@@ -286,7 +286,6 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
     p.M = 6144;
     p.N = n_tok;
     p.splits = sk->splits_qkv;
-    p.kb_per_split = 64 / p.splits;
     p.n_tiles = sk->n_tiles;
     p.m_tiles = 48;
     p.fin0 = q_out;
@@ -303,7 +302,6 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
     p.M = n_tok;
     p.N = 6144;
     p.splits = 1;
-    p.kb_per_split = 64;
     p.n_tiles = 24;
     p.m_tiles = (n_tok + 255) / 256;
     p.out0 = q_out;
@@ -331,7 +329,6 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
     p.M = 4096;
     p.N = n_tok;
     p.splits = sk->splits_o;
-    p.kb_per_split = 64 / p.splits;
     p.n_tiles = sk->n_tiles;
     p.m_tiles = 32;
     p.fin0 = delta;
@@ -344,7 +341,6 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
     p.M = n_tok;
     p.N = 4096;
     p.splits = 1;
-    p.kb_per_split = 64;
     p.n_tiles = 16;
     p.m_tiles = (n_tok + 255) / 256;
     p.out0 = delta;
@@ -483,7 +479,6 @@ gqa_status prefill_impl(gqa_ctx* c, const void* x, int B, int T, const float* R,
   fp.start_pos = start_pos;
   fp.causal = causal ? 1 : 0;
   fp.n_qtiles = (T + 127) / 128;
-  fp.H = h;
   fp.status = c->status;
   fp.scale_log2 = kScaleLog2;
   fp.fault = take_fault(c, GQA_KERNEL_FLASH_PREFILL);

@@ -20,7 +20,6 @@ enum EpiMode : int { kQkvRope = 0, kStoreF32 = 1, kSplitKQkv = 3, kSplitKOut = 4
 struct GemmParams {
   int M, N;          // rows of A, rows of B
   int num_kb;        // K / 64
-  int kb_per_split;  // unused by the kernels (k ranges are split evenly)
   int splits;        // few-token kernel: k splits = cluster size
   int n_tiles;       // ceil(N / BN)
   int m_tiles;       // ceil(M / 128)
@@ -45,7 +44,6 @@ struct FlashParams {
   int B, T, S_max, start_pos, causal;
   int n_qtiles;
   int groups_per_band;  // (sequence, kv group) pairs scheduled together (divides 8 B)
-  void* H;  // [B*T, 4096] bf16
   int* status;
   int fault;  // test hook: CTA 0's producer issues no loads (its waits run out)
   float scale_log2;  // log2(e) / sqrt(128)
