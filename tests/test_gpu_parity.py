@@ -55,6 +55,13 @@ def test_prefill_ragged_shapes(B, T):
     _run_prefill_case(gin.make_custom(seed=100 + T, B=B, T=T))
 
 
+def test_prefill_with_scaled_rope_table():
+    # the Llama 3.1 scaled table is just another R input: same kernels, same oracle
+    inp = gin.make_custom(seed=9, B=2, T=1000)
+    inp.R = gin.rope_table(np.arange(1000), scaled=True)
+    _run_prefill_case(inp)
+
+
 def test_prefill_non_causal():
     _run_prefill_case(gin.make_custom(seed=7, B=2, T=300), causal=False)
 

@@ -468,3 +468,32 @@ def test_planted_norm_mistakes_are_caught(monkeypatch):
         y = orc.rms_norm(np.full((1, 2, 64), c), w, eps)
         assert not np.allclose(y, want, rtol=1e-6)
     monkeypatch.setattr(orc, "rms_norm", good)
+
+
+# ---------------------------------------------------------------- scaled RoPE table (Llama 3.1)
+def test_scaled_frequencies_keep_fast_pairs_and_slow_down_slow_pairs():
+    w = 500000.0 ** (-(2.0 * np.arange(64)) / 128)
+    ws = gin.scaled_frequencies(w)
+    wavelen = 2 * np.pi / w
+    fast = wavelen < 8192 / 4
+    slow = wavelen > 8192 / 1
+    assert fast.any() and slow.any() and (~fast & ~slow).any()
+    np.testing.assert_array_equal(ws[fast], w[fast])
+    np.testing.assert_allclose(ws[slow], w[slow] / 8, rtol=1e-15)
+    mid = ~fast & ~slow
+    assert np.all(ws[mid] < w[mid]) and np.all(ws[mid] > w[mid] / 8)
+    # never faster than the base frequency; the interpolation meets both ends continuously
+    assert np.all(ws <= w)
+    lo = gin.scaled_frequencies(np.array([2 * np.pi / (8192 / 4 + 1e-9), 2 * np.pi / (8192 - 1e-9)]))
+    np.testing.assert_allclose(lo, [2 * np.pi / (8192 / 4), 2 * np.pi / 8192 / 8], rtol=1e-9)
+
+
+def test_scaled_table_rows_are_rotations_and_identity_at_zero():
+    R = gin.rope_table(np.arange(0, 40000, 997), scaled=True).numpy().astype(np.float64)
+    np.testing.assert_allclose(R[..., 0] ** 2 + R[..., 1] ** 2, 1.0, atol=1e-6)
+    np.testing.assert_array_equal(R[0, :, 0], 1.0)
+    np.testing.assert_array_equal(R[0, :, 1], 0.0)
+    # the fastest pair is unscaled, the slowest is 8x slower than unscaled
+    Ru = gin.rope_table(np.arange(0, 40000, 997)).numpy().astype(np.float64)
+    np.testing.assert_array_equal(R[:, 0], Ru[:, 0])
+    assert not np.allclose(R[5:, 63], Ru[5:, 63])

@@ -91,17 +91,43 @@ class BlockInputs:
     meta: dict = field(default_factory=dict)
 
 
-def rope_table(positions, head_dim: int = HEAD_DIM, theta: float = ROPE_THETA) -> torch.Tensor:
-    """Rotation table R[t, j] = (cos(p_t w_j), sin(p_t w_j)), w_j = theta^(-2j/head_dim).
+# Llama 3.1 frequency scaling (the catalogue's use_scaled_rope: True).  The pages show the
+# flag and the scaled frequency w' in the RoPE step but not the rule; this is the rule Meta
+# published with Llama 3.1 (an external reading): wavelengths shorter than the original
+# context / high_freq_factor keep their frequency, those longer than original context /
+# low_freq_factor are slowed by `factor`, and the band in between is interpolated linearly
+# in (original context / wavelength).
+SCALE_FACTOR = 8.0
+SCALE_LOW_FREQ_FACTOR = 1.0
+SCALE_HIGH_FREQ_FACTOR = 4.0
+SCALE_ORIGINAL_CONTEXT = 8192.0
+
+
+def scaled_frequencies(w: np.ndarray) -> np.ndarray:
+    """The Llama 3.1 scaled frequencies w' for base frequencies w (fp64)."""
+    w = np.asarray(w, dtype=np.float64)
+    wavelen = 2.0 * np.pi / w
+    low_wavelen = SCALE_ORIGINAL_CONTEXT / SCALE_LOW_FREQ_FACTOR
+    high_wavelen = SCALE_ORIGINAL_CONTEXT / SCALE_HIGH_FREQ_FACTOR
+    smooth = (SCALE_ORIGINAL_CONTEXT / wavelen - SCALE_LOW_FREQ_FACTOR) / (SCALE_HIGH_FREQ_FACTOR - SCALE_LOW_FREQ_FACTOR)
+    mid = (1.0 - smooth) * w / SCALE_FACTOR + smooth * w
+    return np.where(wavelen < high_wavelen, w, np.where(wavelen > low_wavelen, w / SCALE_FACTOR, mid))
+
+
+def rope_table(positions, head_dim: int = HEAD_DIM, theta: float = ROPE_THETA, scaled: bool = False) -> torch.Tensor:
+    """Rotation table R[t, j] = (cos(p_t w_j), sin(p_t w_j)), w_j = theta^(-2j/head_dim)
+    (with ``scaled``, the Llama 3.1 frequencies scaled_frequencies(w)).
 
     The pages name R as an input of the block ([T positions, 64 pairs]) but do not print
-    its generator; this is the standard unscaled form with the catalogue's theta.  Angles
-    are formed in fp64 and cos/sin rounded once to fp32.  Both the CUDA path and the
+    its generator; the default is the standard unscaled form with the catalogue's theta.
+    Angles are formed in fp64 and cos/sin rounded once to fp32.  Both the CUDA path and the
     oracle read this same array, so the choice of generator does not affect parity.
     """
     p = np.asarray(positions, dtype=np.float64).reshape(-1, 1)
     j = np.arange(head_dim // 2, dtype=np.float64).reshape(1, -1)
     w = theta ** (-(2.0 * j) / head_dim)
+    if scaled:
+        w = scaled_frequencies(w)
     ang = p * w
     out = np.stack([np.cos(ang), np.sin(ang)], axis=-1).astype(np.float32)
     return torch.from_numpy(np.ascontiguousarray(out))
