@@ -40,14 +40,14 @@ int gemm_pair_max_clusters() {
   return n;
 }
 
-cudaError_t launch_gemm_qkv_rope(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                                 int grid, cudaStream_t s) {
-  return launch_pdl(gemm_tc_pair_kernel<6, kQkvRope>, dim3(grid), dim3(192), PairSmem::kBytes, s, 0, a, b, p);
+cudaError_t launch_gemm_qkv_rope(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bt,
+                                 const GemmParams& p, int grid, cudaStream_t s) {
+  return launch_pdl(gemm_tc_pair_kernel<6, kQkvRope>, dim3(grid), dim3(192), PairSmem::kBytes, s, 0, a, b, bt, p);
 }
 
-cudaError_t launch_gemm_store_f32(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                                  int grid, cudaStream_t s) {
-  return launch_pdl(gemm_tc_pair_kernel<6, kStoreF32>, dim3(grid), dim3(192), PairSmem::kBytes, s, 0, a, b, p);
+cudaError_t launch_gemm_store_f32(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bt,
+                                  const GemmParams& p, int grid, cudaStream_t s) {
+  return launch_pdl(gemm_tc_pair_kernel<6, kStoreF32>, dim3(grid), dim3(192), PairSmem::kBytes, s, 0, a, b, bt, p);
 }
 
 // One cluster of p.splits CTAs per 128-feature tile (cluster rank = k split).

@@ -7,7 +7,8 @@
 //     under the main loop of the next.  Warp roles per CTA: warp 0 TMA producer, warp 1
 //     TMEM owner (+ the single UMMA-issuing thread in CTA 0 of the pair), warps 2..5
 //     epilogue.  Tiles are numbered with the n tile fastest so the pairs resident at one
-//     time share A row bands through L2.
+//     time share A row bands through L2; the tiles of a last, partial round are cut along
+//     N into narrower items spread over all pairs (pair_item).
 //   gemm_splitk_cluster_kernel (few tokens) — swap-AB split-K over a thread-block cluster
 //     with the reduction done through distributed shared memory.
 //
@@ -172,6 +173,42 @@ __device__ __forceinline__ void store_f32_chunk(const GemmParams& p, const float
 //   - both CTAs' TMA loads complete on CTA 0's full barrier (CTA 0 expects both halves);
 //   - CTA 0's commits arrive on the empty / accumulator-full barriers of both CTAs;
 //   - each CTA's epilogue warps release an accumulator on CTA 0's acc_empty barrier.
+// Work item idx of a CTA pair: m tile mt, output columns n0 .. n0 + w - 1.  First the whole
+// 256x256 tiles pair + j * n_pairs (n tile fastest), j < full_rounds; then, with tail_w > 0,
+// one piece of the last, partial round: each m row of that round has its remaining columns
+// cut into pieces of tail_w columns (a multiple of 32; the last piece of a row may be
+// narrower), numbered row by row, piece `pair` going to this pair.  So the partial round
+// costs about tail_w / 256 of a tile instead of a whole one, and no pair streams a row band
+// of A twice.  Returns false past the pair's last item.
+__device__ __forceinline__ bool pair_item(const GemmParams& p, int pair, int n_pairs, int idx, int& mt, int& n0,
+                                          int& w) {
+  const int total = p.m_tiles * p.n_tiles;
+  if (p.tail_w == 0 || idx < p.full_rounds) {
+    const int u = pair + idx * n_pairs;
+    mt = u / p.n_tiles;
+    n0 = (u - mt * p.n_tiles) * 256;
+    w = 256;
+    return u < total;
+  }
+  if (idx > p.full_rounds) return false;
+  const int ncols = p.n_tiles * 256;
+  const int base = p.full_rounds * n_pairs;  // first tile of the partial round
+  int r = base / p.n_tiles;
+  int c = (base - r * p.n_tiles) * 256;
+  int q = pair;
+  for (; r < p.m_tiles; ++r, c = 0) {
+    const int k = (ncols - c + p.tail_w - 1) / p.tail_w;
+    if (q < k) {
+      mt = r;
+      n0 = c + q * p.tail_w;
+      w = min(p.tail_w, ncols - n0);
+      return true;
+    }
+    q -= k;
+  }
+  return false;
+}
+
 template <int STAGES>
 struct GemmPairSmem {
   static constexpr int kABytes = 128 * 64 * 2;
@@ -186,7 +223,7 @@ struct GemmPairSmem {
 template <int STAGES, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmBt, const GemmParams p) {
   using L = GemmPairSmem<STAGES>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -207,7 +244,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   const uint32_t rank = cluster_ctarank();
   const int pair = blockIdx.x >> 1;
   const int n_pairs = gridDim.x >> 1;
-  const int total_units = p.m_tiles * p.n_tiles;  // 256x256 tiles, n fastest
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -238,24 +274,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       // ------------------------------------------------------------ TMA producer
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      tma_prefetch_desc(&tmBt);
       int it = 0;
       bool ok = true;
       // B is the context's weight copy (never written after creation): its first stages are
       // fetched before waiting for the previous kernel; A (activations) only after.
       // test hook: pair 0 issues no loads, so CTA 0's issuer waits out and aborts
+      // B rows of an item: CTA r holds rows n0 + w/2 * r .. + w/2 - 1 of the weight, fetched as
+      // one box per stage: 128 rows for a whole tile (tmB), tail_w / 2 rows for a piece of the
+      // partial round (tmBt; rows past the piece are not read by the UMMA, rows past the
+      // weight are zero-filled).  CTA 0's barrier counts both CTAs' A and B boxes.
       const bool no_loads = p.fault && pair == 0;
-      const int n_pre = (pair < total_units && !no_loads) ? min(STAGES, p.num_kb) : 0;
-      if (n_pre > 0) {
-        const int n0 = (pair % p.n_tiles) * 256 + 128 * rank;
-        for (int i = 0; i < n_pre; ++i) {
-          if (rank == 0) mbar_arrive_expect_tx(&full_bar[i], 2 * L::kStageBytes);
-          tma_load_3d_pair(sB + i * L::kBBytes, &tmB, mapa_shared(smem_u32(&full_bar[i]), 0), 0, n0, i);
-        }
+      auto load_b = [&](int st, uint32_t bar, int n0, int w, int kb) {
+        if (w == 256)
+          tma_load_3d_pair(sB + st * L::kBBytes, &tmB, bar, 0, n0 + 128 * static_cast<int>(rank), kb);
+        else
+          tma_load_3d_pair(sB + st * L::kBBytes, &tmBt, bar, 0, n0 + (w >> 1) * static_cast<int>(rank), kb);
+      };
+      auto stage_tx = [&](int w) { return 2 * (L::kABytes + 64 * (w == 256 ? 256 : p.tail_w)); };
+      int mt, n0, w;
+      const int n_pre = (pair_item(p, pair, n_pairs, 0, mt, n0, w) && !no_loads) ? min(STAGES, p.num_kb) : 0;
+      for (int i = 0; i < n_pre; ++i) {
+        if (rank == 0) mbar_arrive_expect_tx(&full_bar[i], stage_tx(w));
+        load_b(i, mapa_shared(smem_u32(&full_bar[i]), 0), n0, w, i);
       }
       griddep_wait();
-      for (int u = pair; ok && !no_loads && u < total_units; u += n_pairs) {
-        const int m0 = (u / p.n_tiles) * 256 + 128 * rank;
-        const int n0 = (u % p.n_tiles) * 256 + 128 * rank;
+      for (int idx = 0; ok && !no_loads && pair_item(p, pair, n_pairs, idx, mt, n0, w); ++idx) {
+        const int m0 = mt * 256 + 128 * rank;
         for (int i = 0; i < p.num_kb; ++i, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -268,9 +313,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             ok = false;
             break;
           }
-          if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * L::kStageBytes);
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], stage_tx(w));
           tma_load_3d_pair(sA + s * L::kABytes, &tmA, bar0, 0, m0, i);
-          tma_load_3d_pair(sB + s * L::kBBytes, &tmB, bar0, 0, n0, i);
+          load_b(s, bar0, n0, w, i);
         }
       }
       if (*abort_flag && rank == 0) {  // CTA 0's barriers count both CTAs' bytes
@@ -282,13 +327,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     if (rank == 0) {
       // ------------------------------------------------------------ UMMA issuer (CTA 0)
       // The whole warp runs the loop (waits are warp-uniform); one elected lane issues.
-      constexpr uint32_t idesc = idesc_bf16_f32(256, 256, 0, 0);
       const uint32_t a_base = smem_u32(sA);
       const uint32_t b_base = smem_u32(sB);
       int it = 0, lt = 0;
       bool ok = true;
-      for (int u = pair; ok && u < total_units; u += n_pairs, ++lt) {
+      int mt, n0, w;
+      for (; ok && pair_item(p, pair, n_pairs, lt, mt, n0, w); ++lt) {
         const int ab = lt & 1;
+        const uint32_t idesc = idesc_bf16_f32(256, w, 0, 0);
         if (!(ok = __all_sync(0xffffffffu, mbar_wait_cluster(&acc_empty[ab], ((lt >> 1) & 1) ^ 1u, abort_flag,
                                                              p.status))))
           break;
@@ -326,29 +372,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     float* stage = reinterpret_cast<float*>(smem + L::kEpiOffset) + (warp - 2) * kEpiWarpFloats;
     int lt = 0;
-    for (int u = pair; u < total_units; u += n_pairs, ++lt) {
+    int mt, n0, w;
+    for (; pair_item(p, pair, n_pairs, lt, mt, n0, w); ++lt) {
       const int ab = lt & 1;
-      const int m_base = (u / p.n_tiles) * 256 + 128 * rank + quarter * 32;
-      const int n0 = (u % p.n_tiles) * 256;
-      // Q/K tiles: all rotation coefficients of the tile are read before waiting for the
-      // accumulator, so their latency hides under the main loop (chunks cp and cp + 4, the
-      // tile's two 128-column head slices, share RoPE pairs)
+      const int m_base = mt * 256 + 128 * rank + quarter * 32;
+      // The item's 32-column chunks i = 0 .. w/32 - 1 sit at accumulator columns 32 i and
+      // output columns n0 + 32 i; pass cp stores chunks cp and cp + 4, which lie 128 columns
+      // (one head slice) apart and so rotate by the same RoPE pairs, those of position
+      // ((n0 / 32) + cp) mod 4 of a head slice.  Q/K items read all their rotation
+      // coefficients before waiting for the accumulator, so the latency hides under the main
+      // loop.
       const bool rope = EPI == kQkvRope && n0 < 5120;
       QkvRows qr{};
       float4 cs[4][4][2];
-      // Delta tiles with a residual: the residual of chunk pair cp + 1 is read while pair cp
+      // Delta items with a residual: the residual of chunk pair cp + 1 is read while pair cp
       // is stored (pair 0 before the accumulator wait)
       uint2 rva[8], rvb[8], rva_n[8], rvb_n[8];
       if constexpr (EPI == kQkvRope) {
         qr = qkv_rows(p, lane, m_base);
         if (rope) {
 #pragma unroll
-          for (int cp = 0; cp < 4; ++cp) load_rope(p, qr, lane, cp, cs[cp]);
+          for (int cp = 0; cp < 4; ++cp) load_rope(p, qr, lane, ((n0 >> 5) + cp) & 3, cs[cp]);
         }
       } else {
         if (p.residual) {
           load_residual_chunk(p, lane, m_base, n0, rva);
-          load_residual_chunk(p, lane, m_base, n0 + 128, rvb);
+          if (w > 128) load_residual_chunk(p, lane, m_base, n0 + 128, rvb);
         }
       }
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[ab], (lt >> 1) & 1, abort_flag, p.status));
@@ -357,15 +406,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       const uint32_t t_row = tmem_base + lane_off + ab * 256;
 #pragma unroll
       for (int cp = 0; cp < 4; ++cp) {
+        const bool has_a = 32 * cp < w, has_b = 32 * (cp + 4) < w;
         if constexpr (EPI == kStoreF32) {
           if (p.residual && cp < 3) {
-            load_residual_chunk(p, lane, m_base, n0 + (cp + 1) * 32, rva_n);
-            load_residual_chunk(p, lane, m_base, n0 + (cp + 5) * 32, rvb_n);
+            if (32 * (cp + 1) < w) load_residual_chunk(p, lane, m_base, n0 + (cp + 1) * 32, rva_n);
+            if (32 * (cp + 5) < w) load_residual_chunk(p, lane, m_base, n0 + (cp + 5) * 32, rvb_n);
           }
         }
+        if (!has_a) break;  // chunks are filled in order: none left
         uint32_t va[32], vb[32];
         tmem_ld32(t_row + cp * 32, va);
-        tmem_ld32(t_row + (cp + 4) * 32, vb);
+        if (has_b) tmem_ld32(t_row + (cp + 4) * 32, vb);
         tmem_ld_wait();
         stage_chunk(stage, lane, va);
         __syncwarp();
@@ -375,14 +426,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           store_f32_chunk(p, stage, lane, m_base, n0 + cp * 32, rva);
         }
         __syncwarp();
-        stage_chunk(stage, lane, vb);
-        __syncwarp();
-        if constexpr (EPI == kQkvRope) {
-          store_qkv_chunk(p, stage, lane, qr, n0 + (cp + 4) * 32, cs[cp]);
-        } else {
-          store_f32_chunk(p, stage, lane, m_base, n0 + (cp + 4) * 32, rvb);
+        if (has_b) {
+          stage_chunk(stage, lane, vb);
+          __syncwarp();
+          if constexpr (EPI == kQkvRope) {
+            store_qkv_chunk(p, stage, lane, qr, n0 + (cp + 4) * 32, cs[cp]);
+          } else {
+            store_f32_chunk(p, stage, lane, m_base, n0 + (cp + 4) * 32, rvb);
+          }
+          __syncwarp();
         }
-        __syncwarp();
         if constexpr (EPI == kStoreF32) {
           if (p.residual && cp < 3) {
 #pragma unroll

@@ -267,6 +267,34 @@ struct ProfScope {
 const float kScaleLog2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
 
 // Q/K/V projection + RoPE + cache write for n_tok tokens laid out [B, T] (steps 1-5).
+// Schedule of the CTA-pair GEMM over n_pairs co-resident pairs (p.m_tiles x p.n_tiles tiles
+// of 256 x 256, n fastest): whole tiles round-robin; when the last round is partial, each of
+// its m rows has its remaining columns cut into pieces of tail_w columns, one piece per pair,
+// tail_w the smallest multiple of 32 for which the pieces of all those rows fit the pairs
+// (the kernel's pair_item walks the same rows).  Returns the grid size in CTAs.
+int plan_pair_grid(GemmParams& p, int n_pairs) {
+  const int total = p.m_tiles * p.n_tiles;
+  const int ncols = p.n_tiles * 256;
+  p.full_rounds = total / n_pairs;
+  p.tail_w = 0;
+  const int base = p.full_rounds * n_pairs;
+  if (base == total) return 2 * n_pairs;
+  auto pieces = [&](int w) {
+    int n = 0;
+    for (int r = base / p.n_tiles, c = (base % p.n_tiles) * 256; r < p.m_tiles; ++r, c = 0)
+      n += (ncols - c + w - 1) / w;
+    return n;
+  };
+  for (int w = 32; w < 256; w += 32) {
+    if (pieces(w) <= n_pairs) {
+      p.tail_w = w;
+      break;
+    }
+  }
+  if (p.tail_w == 0) return 2 * std::min(total, n_pairs);
+  return 2 * (p.full_rounds > 0 ? n_pairs : pieces(p.tail_w));
+}
+
 gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, void* ck, void* cv,
                    int S_max, int start_pos, void* q_out, const WsLayout& w, const SkinnyPlan* sk,
                    const float* row_scale, cudaStream_t s) {
@@ -308,9 +336,11 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
     p.out1 = ck;
     p.out2 = cv;
     p.R = R;
-    const int grid = 2 * std::min(p.m_tiles * p.n_tiles, c->pair_clusters);
+    const int grid = plan_pair_grid(p, c->pair_clusters);
+    CUtensorMap tbt = tb;  // boxes of tail_w / 2 rows for the pieces of a partial last round
+    if (p.tail_w && !map_weight_tiled(&tbt, wqkv, 6144, p.tail_w / 2)) return cuda_fail(cudaErrorInvalidValue);
     p.fault = take_fault(c, GQA_KERNEL_QKV_GEMM);
-    { ProfScope ps(c, GQA_KERNEL_QKV_GEMM, s); GQA_CUDA(launch_gemm_qkv_rope(ta, tb, p, grid, s)); }
+    { ProfScope ps(c, GQA_KERNEL_QKV_GEMM, s); GQA_CUDA(launch_gemm_qkv_rope(ta, tb, tbt, p, grid, s)); }
   }
   return GQA_OK;
 }
@@ -345,9 +375,11 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
     p.m_tiles = (n_tok + 255) / 256;
     p.out0 = delta;
     p.ldo = 4096;
-    const int grid = 2 * std::min(p.m_tiles * p.n_tiles, c->pair_clusters);
+    const int grid = plan_pair_grid(p, c->pair_clusters);
+    CUtensorMap tbt = tb;
+    if (p.tail_w && !map_weight_tiled(&tbt, c->w_o, 4096, p.tail_w / 2)) return cuda_fail(cudaErrorInvalidValue);
     p.fault = take_fault(c, GQA_KERNEL_OUT_GEMM);
-    { ProfScope ps(c, GQA_KERNEL_OUT_GEMM, s); GQA_CUDA(launch_gemm_store_f32(ta, tb, p, grid, s)); }
+    { ProfScope ps(c, GQA_KERNEL_OUT_GEMM, s); GQA_CUDA(launch_gemm_store_f32(ta, tb, tbt, p, grid, s)); }
   }
   return GQA_OK;
 }

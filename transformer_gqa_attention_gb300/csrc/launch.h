@@ -51,10 +51,12 @@ cudaError_t configure_kernels();
 // Number of 2-CTA clusters of the pair GEMM that can be resident at once (0 on error).
 int gemm_pair_max_clusters();
 
-cudaError_t launch_gemm_qkv_rope(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                                 int grid, cudaStream_t s);
-cudaError_t launch_gemm_store_f32(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                                  int grid, cudaStream_t s);
+// b: weight map with 128-row boxes (whole tiles); bt: the same weight, p.tail_w / 2-row boxes
+// (pieces of a partial last round)
+cudaError_t launch_gemm_qkv_rope(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bt,
+                                 const GemmParams& p, int grid, cudaStream_t s);
+cudaError_t launch_gemm_store_f32(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bt,
+                                  const GemmParams& p, int grid, cudaStream_t s);
 // Few-token split-K projections with the reduction fused (last split of each tile).
 cudaError_t launch_gemm_splitk_qkv(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                                    int grid, cudaStream_t s);

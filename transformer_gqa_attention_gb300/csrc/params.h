@@ -23,6 +23,9 @@ struct GemmParams {
   int splits;        // few-token kernel: k splits = cluster size
   int n_tiles;       // ceil(N / BN)
   int m_tiles;       // ceil(M / 128)
+  // CTA-pair kernel schedule: full_rounds rounds of whole 256x256 tiles, then the tiles of
+  // the last, partial round cut into pieces of tail_w columns (0: whole tiles throughout)
+  int full_rounds, tail_w;
   // epilogue operands
   void* out0;        // kQkvRope: Q_r [M,4096] bf16 | kStoreF32: D fp32
   void* out1;        // kQkvRope: cache_k
