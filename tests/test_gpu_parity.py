@@ -70,6 +70,30 @@ def test_prefill_b1_t2048_workload_full():
     _run_prefill_case(gin.make_inputs("prefill_b1_t2048"), check_intermediates=False)
 
 
+def test_prefill_narrow_last_round_pieces():
+    # 4096 tokens: the Q/K/V projection's 384 tiles of 256 x 256 leave 4 (the V columns of the
+    # last 256 rows) for a partial last round, cut into 32-column pieces (N = 32 UMMAs, 16-row
+    # weight boxes); W_O's 256 tiles leave 28 (rows 3584..4095), cut into 96-column pieces.
+    # K_r and V are checked in full, Q_r, H and Delta on sampled rows that include those rows.
+    B, T = 1, 4096
+    inp = gin.make_custom(seed=41, B=B, T=T)
+    blk = gu.Block(inp)
+    try:
+        ck, cv = gu.empty_cache(B, T)
+        delta = blk.prefill(inp.x.to(gu.DEV), inp.R.to(gu.DEV), ck, cv)
+        rows = np.union1d(gu.sample_rows(T), np.arange(3584, T, 9))
+        ref, ex = gu.oracle_prefill(blk, inp, rows=rows, keep=True)
+        q_r, h = blk.intermediates(B * T)
+        gu.assert_close(gu.np64(ck), ex["K_r"], gu.TOL_BF16_REL_L1, gu.TOL_BF16_MAX, "K_r")
+        gu.assert_close(gu.np64(cv), ex["V"], gu.TOL_BF16_REL_L1, gu.TOL_BF16_MAX, "V")
+        gu.assert_close(gu.np64(q_r).reshape(B, T, 32, 128)[:, rows], ex["Q_r"], gu.TOL_BF16_REL_L1,
+                        gu.TOL_BF16_MAX, "Q_r rows")
+        gu.assert_close(gu.np64(h).reshape(B, T, 4096)[:, rows], ex["H"], gu.TOL_REL_L1, gu.TOL_MAX, "H rows")
+        gu.assert_close(gu.np64(delta[:, rows]), ref, what="delta rows")
+    finally:
+        blk.close()
+
+
 @pytest.mark.parametrize("name", ["prefill_b4_t8192", "prefill_b1_t32768"])
 def test_prefill_large_workloads_sampled_rows(name):
     inp = gin.make_inputs(name)
