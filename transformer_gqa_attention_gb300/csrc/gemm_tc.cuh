@@ -13,8 +13,9 @@
 //     with the reduction done through distributed shared memory.
 //
 // Operands are read through 3-D tensor maps (64 columns, rows, 64-column k block), box
-// 64 x {64,128} x 1, so the same kernels read row-major activations (k-block stride 128 B)
-// and the k-block-major weight copies the context keeps (each box one contiguous 16 KB).
+// 64 x {64,128} x 1 (and 64 x tail_w/2 x 1 for the weight rows of a last-round piece), so
+// the same kernels read row-major activations (k-block stride 128 B) and the k-block-major
+// weight copies the context keeps (each 128-row box one contiguous 16 KB).
 //
 // Epilogues:
 //   kQkvRope  — the fused Q/K/V projection (steps 1-5 of "Llama 3.1 8B · Grouped-query
