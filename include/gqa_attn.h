@@ -256,6 +256,22 @@ gqa_status attn_decode_attention_noalloc(const void *q_r, const void *cache_k,
  */
 gqa_status attn_debug_inject_timeout(gqa_ctx *ctx, int kind);
 
+/*
+ * attn_debug_pair_schedule — the work schedule of the many-token projection GEMM, computed
+ * on the host exactly as the library sizes a launch and as each CTA pair walks it (no
+ * counterpart on the pages; for tests, no GPU needed).  Output tiles of 256 x 256:
+ * m_tiles x n_tiles of them (n_tiles 24 for the Q/K/V projection, 16 for W_O), over n_pairs
+ * co-resident CTA pairs.  Writes *full_rounds (rounds of whole tiles), *tail_w (width of the
+ * pieces the last, partial round is cut into; 0: none) and *grid_ctas (CTAs launched), and
+ * the items in launch order of pairs, each pair's items in the order it runs them, as
+ * quadruples (pair, m tile, first column, width) into items[4 * max_items]; *n_items gets
+ * their count.  Errors: GQA_ERR_INVALID_ARG (null pointer, m_tiles, n_tiles or n_pairs < 1,
+ * max_items < 0), GQA_ERR_SHAPE (more than max_items items; *n_items holds the count).
+ */
+gqa_status attn_debug_pair_schedule(int m_tiles, int n_tiles, int n_pairs, int *full_rounds,
+                                    int *tail_w, int *grid_ctas, int *items, int max_items,
+                                    int *n_items);
+
 /* attn_destroy — free everything the context owns (after synchronising the device).
  * NULL is ignored. */
 void attn_destroy(gqa_ctx *ctx);

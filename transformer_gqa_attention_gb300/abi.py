@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "GQA_OK", 1: "GQA_ERR_INVALID_ARG", 2: "GQA_ERR_SHAPE", 3: "G
 EXPORTED = ("attn_create", "attn_prefill", "attn_decode", "attn_set_norm", "attn_prefill_residual",
             "attn_decode_residual", "attn_sync_status", "attn_debug_buffers",
             "attn_profile_begin", "attn_profile_end", "attn_debug_inject_timeout",
-            "attn_decode_attention_noalloc",
+            "attn_debug_pair_schedule", "attn_decode_attention_noalloc",
             "attn_destroy", "attn_strerror", "attn_last_cuda_error")
 
 # Kernel kinds of attn_profile_end (GQA_KERNEL_* in include/gqa_attn.h).
@@ -72,6 +72,9 @@ def lib() -> ctypes.CDLL:
     L.attn_profile_end.restype = i32
     L.attn_debug_inject_timeout.argtypes = [vp, i32]
     L.attn_debug_inject_timeout.restype = i32
+    ip = ctypes.POINTER(i32)
+    L.attn_debug_pair_schedule.argtypes = [i32, i32, i32, ip, ip, ip, ip, i32, ip]
+    L.attn_debug_pair_schedule.restype = i32
     L.attn_decode_attention_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
     L.attn_decode_attention_noalloc.restype = i32
     L.attn_destroy.argtypes = [vp]
@@ -162,6 +165,25 @@ def attn_profile_end(ctx, stream=None):
     cnt = (ctypes.c_int * n)()
     _check("attn_profile_end", lib().attn_profile_end(ctx, ms, cnt, _stream(stream)))
     return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def attn_debug_pair_schedule(m_tiles, n_tiles, n_pairs):
+    """The many-token projection GEMM's work schedule (host computation, no GPU needed):
+    (full_rounds, tail_w, grid_ctas, items) with items a list of (pair, m tile, first column,
+    width) in launch order."""
+    i32 = ctypes.c_int
+    full, tail, grid, n = i32(), i32(), i32(), i32()
+    L = lib()
+    st = L.attn_debug_pair_schedule(m_tiles, n_tiles, n_pairs, ctypes.byref(full), ctypes.byref(tail),
+                                    ctypes.byref(grid), None, 0, ctypes.byref(n))
+    if st not in (0, 2):  # GQA_ERR_SHAPE: the count is in n
+        _check("attn_debug_pair_schedule", st)
+    buf = (i32 * (4 * max(n.value, 1)))()
+    _check("attn_debug_pair_schedule",
+           L.attn_debug_pair_schedule(m_tiles, n_tiles, n_pairs, ctypes.byref(full), ctypes.byref(tail),
+                                      ctypes.byref(grid), buf, n.value, ctypes.byref(n)))
+    items = [tuple(buf[4 * i:4 * i + 4]) for i in range(n.value)]
+    return full.value, tail.value, grid.value, items
 
 
 def attn_debug_inject_timeout(ctx, kind):

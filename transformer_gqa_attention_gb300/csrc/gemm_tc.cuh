@@ -27,6 +27,7 @@
 //   kSplitKQkv / kSplitKOut — the same two epilogues for the few-token kernel.
 #pragma once
 
+#include "pair_sched.h"
 #include "params.h"
 #include "ptx.cuh"
 
@@ -174,42 +175,6 @@ __device__ __forceinline__ void store_f32_chunk(const GemmParams& p, const float
 //   - both CTAs' TMA loads complete on CTA 0's full barrier (CTA 0 expects both halves);
 //   - CTA 0's commits arrive on the empty / accumulator-full barriers of both CTAs;
 //   - each CTA's epilogue warps release an accumulator on CTA 0's acc_empty barrier.
-// Work item idx of a CTA pair: m tile mt, output columns n0 .. n0 + w - 1.  First the whole
-// 256x256 tiles pair + j * n_pairs (n tile fastest), j < full_rounds; then, with tail_w > 0,
-// one piece of the last, partial round: each m row of that round has its remaining columns
-// cut into pieces of tail_w columns (a multiple of 32; the last piece of a row may be
-// narrower), numbered row by row, piece `pair` going to this pair.  So the partial round
-// costs about tail_w / 256 of a tile instead of a whole one, and no pair streams a row band
-// of A twice.  Returns false past the pair's last item.
-__device__ __forceinline__ bool pair_item(const GemmParams& p, int pair, int n_pairs, int idx, int& mt, int& n0,
-                                          int& w) {
-  const int total = p.m_tiles * p.n_tiles;
-  if (p.tail_w == 0 || idx < p.full_rounds) {
-    const int u = pair + idx * n_pairs;
-    mt = u / p.n_tiles;
-    n0 = (u - mt * p.n_tiles) * 256;
-    w = 256;
-    return u < total;
-  }
-  if (idx > p.full_rounds) return false;
-  const int ncols = p.n_tiles * 256;
-  const int base = p.full_rounds * n_pairs;  // first tile of the partial round
-  int r = base / p.n_tiles;
-  int c = (base - r * p.n_tiles) * 256;
-  int q = pair;
-  for (; r < p.m_tiles; ++r, c = 0) {
-    const int k = (ncols - c + p.tail_w - 1) / p.tail_w;
-    if (q < k) {
-      mt = r;
-      n0 = c + q * p.tail_w;
-      w = min(p.tail_w, ncols - n0);
-      return true;
-    }
-    q -= k;
-  }
-  return false;
-}
-
 template <int STAGES>
 struct GemmPairSmem {
   static constexpr int kABytes = 128 * 64 * 2;

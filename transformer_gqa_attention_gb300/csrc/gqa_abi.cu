@@ -14,6 +14,7 @@
 
 #include "gqa_attn.h"
 #include "launch.h"
+#include "pair_sched.h"
 #include "params.h"
 
 using namespace gqa;
@@ -267,34 +268,6 @@ struct ProfScope {
 const float kScaleLog2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
 
 // Q/K/V projection + RoPE + cache write for n_tok tokens laid out [B, T] (steps 1-5).
-// Schedule of the CTA-pair GEMM over n_pairs co-resident pairs (p.m_tiles x p.n_tiles tiles
-// of 256 x 256, n fastest): whole tiles round-robin; when the last round is partial, each of
-// its m rows has its remaining columns cut into pieces of tail_w columns, one piece per pair,
-// tail_w the smallest multiple of 32 for which the pieces of all those rows fit the pairs
-// (the kernel's pair_item walks the same rows).  Returns the grid size in CTAs.
-int plan_pair_grid(GemmParams& p, int n_pairs) {
-  const int total = p.m_tiles * p.n_tiles;
-  const int ncols = p.n_tiles * 256;
-  p.full_rounds = total / n_pairs;
-  p.tail_w = 0;
-  const int base = p.full_rounds * n_pairs;
-  if (base == total) return 2 * n_pairs;
-  auto pieces = [&](int w) {
-    int n = 0;
-    for (int r = base / p.n_tiles, c = (base % p.n_tiles) * 256; r < p.m_tiles; ++r, c = 0)
-      n += (ncols - c + w - 1) / w;
-    return n;
-  };
-  for (int w = 32; w < 256; w += 32) {
-    if (pieces(w) <= n_pairs) {
-      p.tail_w = w;
-      break;
-    }
-  }
-  if (p.tail_w == 0) return 2 * std::min(total, n_pairs);
-  return 2 * (p.full_rounds > 0 ? n_pairs : pieces(p.tail_w));
-}
-
 gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, void* ck, void* cv,
                    int S_max, int start_pos, void* q_out, const WsLayout& w, const SkinnyPlan* sk,
                    const float* row_scale, cudaStream_t s) {
@@ -668,6 +641,34 @@ gqa_status attn_debug_inject_timeout(gqa_ctx* c, int kind) {
     default:
       return GQA_ERR_INVALID_ARG;
   }
+}
+
+gqa_status attn_debug_pair_schedule(int m_tiles, int n_tiles, int n_pairs, int* full_rounds, int* tail_w,
+                                    int* grid_ctas, int* items, int max_items, int* n_items) {
+  if (!full_rounds || !tail_w || !grid_ctas || !n_items || (!items && max_items > 0) || m_tiles < 1 ||
+      n_tiles < 1 || n_pairs < 1 || max_items < 0)
+    return GQA_ERR_INVALID_ARG;
+  GemmParams p{};
+  p.m_tiles = m_tiles;
+  p.n_tiles = n_tiles;
+  const int grid = plan_pair_grid(p, n_pairs);
+  *full_rounds = p.full_rounds;
+  *tail_w = p.tail_w;
+  *grid_ctas = grid;
+  int n = 0;
+  for (int pair = 0; pair < grid / 2; ++pair) {
+    int mt, n0, w;
+    for (int idx = 0; pair_item(p, pair, grid / 2, idx, mt, n0, w); ++idx, ++n) {
+      if (n < max_items) {
+        items[4 * n + 0] = pair;
+        items[4 * n + 1] = mt;
+        items[4 * n + 2] = n0;
+        items[4 * n + 3] = w;
+      }
+    }
+  }
+  *n_items = n;
+  return n > max_items ? GQA_ERR_SHAPE : GQA_OK;
 }
 
 gqa_status attn_profile_begin(gqa_ctx* c) {
