@@ -1,13 +1,19 @@
 #!/usr/bin/env python
 """Benchmark of the GB300 grouped-query attention block forward; prints ONE JSON line.
 
-Default workload: prefill of B=1 sequence of T=2048 tokens (dim 4096, 32 q / 8 kv heads,
-d_h 128, bf16 inputs, random N(0, 0.02) weights, theta=500000 RoPE table, causal mask,
-fp32 output).  A step is one full block forward (Q/K/V projection + RoPE + cache write,
-causal GQA attention, W_O projection) through the C ABI, inputs resident in HBM.  L2 is
-flushed (256 MiB write) before every timed step, outside the step's events.
+Headline workload: long-context prefill of B=1 sequence of T=32768 tokens (dim 4096, 32 q /
+8 kv heads, d_h 128, bf16 inputs, random N(0, 0.02) weights, theta=500000 RoPE table,
+causal mask, fp32 output).  A step is one full block forward (Q/K/V projection + RoPE +
+cache write, causal GQA attention, W_O projection) through the C ABI, inputs resident in
+HBM.  L2 is flushed (256 MiB write) before every timed step, outside the step's events.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+The same line carries, under "sub_records", one fully measured record (its own step time,
+roofline of the dominant kernel, e2e and clocks, timed in the same process) for each other
+workload of the block: prefill B=1 x T=16, B=1 x T=2048, B=4 x T=8192 and the decode step
+of B=64 sequences at position 4095.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--no-sub]
+                  [--impl reference]
 
 N > 1 runs under torchrun: one rank per GPU, each rank runs its own replica of the
 workload (weak scaling; the path has no cross-sequence exchange), max time over ranks.
@@ -226,33 +232,87 @@ def cores():
         return os.cpu_count()
 
 
-def cpu_baseline(inp, w: gin.Workload, budget_s=15.0):
-    """Time the oracle as it stands on the host cores on a bounded sample (~budget_s)."""
-    w64 = [gin.to_f64(t) for t in (inp.wq, inp.wk, inp.wv, inp.wo)]
-    if w.kind == "prefill":
-        n = min(w.T, 2048)
-        seqs = 1
-        desc = f"oracle prefill of positions 0..{n - 1} of sequence 0"
-    else:
-        n = 1
-        seqs = min(w.B, 4)
-        desc = f"oracle decode of {seqs} of the {w.B} sequences"
+def _oracle_rate(inp, w: gin.Workload, n, seqs, w64, budget_s, max_runs=10):
+    """Repeat the oracle on one bounded sample until budget_s has passed (at most max_runs);
+    return (total seconds, runs, units per run)."""
     times, units = [], 0
     t_start = time.perf_counter()
     while True:
         dt, u = oracle_sample_step(inp, w, n, seqs, w64)
         times.append(dt)
-        units += u
-        if time.perf_counter() - t_start > budget_s or len(times) >= 10:
+        units = u
+        if time.perf_counter() - t_start > budget_s or len(times) >= max_runs:
             break
-    total = sum(times)
+    return sum(times), len(times), units
+
+
+def cpu_baseline(inp, w: gin.Workload, budget_s=15.0):
+    """Time the oracle as it stands on the host cores on a bounded sample (~budget_s).
+
+    Prefill: a causal prefix of sequence 0 (the exact computation of those rows).  When the
+    workload is longer than the prefix, the oracle's time is also extrapolated to the full
+    length from two prefix lengths with t(n) = a n + b n^2 (projections grow with n, the
+    attention products with n^2), and labelled as an extrapolation."""
+    w64 = [gin.to_f64(t) for t in (inp.wq, inp.wk, inp.wv, inp.wo)]
     if w.kind == "prefill":
-        value, unit = units / total, "tokens/s"
-    else:
-        per_seq = decode_bytes(1, w.start_pos + 1) - 41_943_040 * 2
-        value, unit = (len(times) * (seqs * per_seq + 41_943_040 * 2)) / total / 1e9, "GB/s"
-    return {"value": value, "unit": unit, "cores": cores(), "kind": "oracle",
-            "sample": f"{desc}, {len(times)} run(s), {total:.1f} s"}
+        n = min(w.T, 2048)
+        total, runs, u = _oracle_rate(inp, w, n, 1, w64, budget_s)
+        out = {"value": runs * u / total, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+               "sample": f"oracle prefill of positions 0..{n - 1} of sequence 0, {runs} run(s), {total:.1f} s"}
+        if w.T > n:
+            n1 = n // 2
+            t1, r1, _ = _oracle_rate(inp, w, n1, 1, w64, budget_s / 3, max_runs=3)
+            ta, tb = t1 / r1, total / runs
+            # t(n) = a n + b n^2 through (n1, ta) and (n, tb); if the fit gives a negative
+            # coefficient (timing noise, cache effects), the pure quadratic through the longer
+            # prefix, which is the smaller of the two for any non-decreasing cost per pair
+            b = (tb / n - ta / n1) / (n - n1)
+            a = ta / n1 - b * n1
+            if a > 0 and b > 0:
+                t_full = w.B * (a * w.T + b * w.T * w.T)
+                how = f"t(n) = a n + b n^2 fitted to the oracle's times at n = {n1} and {n}"
+            else:
+                t_full = w.B * tb * (w.T / n) ** 2
+                how = f"t(n) = t({n}) (n / {n})^2 (a two-point fit at n = {n1}, {n} gave a negative term)"
+            out["extrapolated_full_workload"] = {
+                "value": w.n_tok / t_full, "unit": "tokens/s", "seconds": t_full,
+                "how": how + f", evaluated at T = {w.T} for {w.B} sequence(s); an extrapolation, not a run"}
+        return out
+    seqs = min(w.B, 4)
+    total, runs, _ = _oracle_rate(inp, w, 1, seqs, w64, budget_s)
+    per_seq = decode_bytes(1, w.start_pos + 1) - 41_943_040 * 2
+    value = runs * (seqs * per_seq + 41_943_040 * 2) / total / 1e9
+    return {"value": value, "unit": "GB/s", "cores": cores(), "kind": "oracle",
+            "sample": f"oracle decode of {seqs} of the {w.B} sequences, {runs} run(s), {total:.1f} s"}
+
+
+SINGLE_CORE_WORKLOADS = ("prefill_b1_t16", "decode_b64_pos4095")
+
+
+def single_core_baseline(name: str, budget_s=4.0):
+    """The oracle on ONE host core (BLAS threads 1, affinity one core) on the workload, in a
+    child process so that the thread settings take effect before numpy loads."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", GQA_BENCH_ONE_CORE="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-one-core", name, "--one-core-budget", str(budget_s)]
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return {"error": (r.stderr.strip().splitlines() or ["failed"])[-1]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def _one_core_child(name: str, budget_s: float):
+    try:
+        os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
+    except (AttributeError, OSError):
+        pass
+    torch.set_num_threads(1)
+    w = gin.WORKLOADS[name]
+    inp = gin.make_inputs(w)
+    rec = cpu_baseline(inp, w, budget_s=budget_s)
+    rec["cores"] = cores()
+    rec["workload"] = name
+    print(json.dumps(rec))
 
 
 def run_reference(args, w, inp):
@@ -303,11 +363,12 @@ def workload_config(w: gin.Workload):
 
 
 # ------------------------------------------------------------------ GPU arm
-def run_gpu(args, w: gin.Workload, inp, world, rank, local):
-    from transformer_gqa_attention_gb300 import _build, abi
+def measure_gpu(args, w: gin.Workload, inp, world, rank, local, steps, warmup):
+    """Time one workload on this rank's GPU: the device-timed steps, a profiled pass of the
+    same steps (per-kernel times) and the end-to-end pass through pinned host buffers.
+    Returns the workload's record on rank 0 (None elsewhere)."""
+    from transformer_gqa_attention_gb300 import abi
     dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    _build.build()
     B, T = w.B, w.T
     S_max = w.s_max
     wts = [t.to(dev) for t in (inp.wq, inp.wk, inp.wv, inp.wo)]
@@ -341,7 +402,7 @@ def run_gpu(args, w: gin.Workload, inp, world, rank, local):
             fn(c, xd, B, w.start_pos, Rd, ck, cv, S_max, out, stream)
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush.zero_()
         step()
     abi.attn_sync_status(ctx, stream)
@@ -350,11 +411,11 @@ def run_gpu(args, w: gin.Workload, inp, world, rank, local):
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
-    for i in range(args.steps):
+    for i in range(steps):
         flush.zero_()
         starts[i].record(stream)
         step()
@@ -371,7 +432,7 @@ def run_gpu(args, w: gin.Workload, inp, world, rank, local):
     # (recorded between launches, so consecutive kernels no longer overlap here)
     torch.cuda.synchronize(dev)
     abi.attn_profile_begin(ctx)
-    for i in range(args.steps):
+    for i in range(steps):
         flush.zero_()
         step()
     prof = abi.attn_profile_end(ctx, stream)
@@ -383,6 +444,7 @@ def run_gpu(args, w: gin.Workload, inp, world, rank, local):
     # Instead of an L2 flush (a device-timing artefact) consecutive steps alternate between
     # two contexts holding separate weight copies (2 x 84 MB > L2), so no step finds the
     # previous step's weights in L2.
+    del flush
     ctx_alt = new_ctx()
     ctxs = (ctx, ctx_alt)
     x_h = inp.x.pin_memory()
@@ -393,9 +455,9 @@ def run_gpu(args, w: gin.Workload, inp, world, rank, local):
     o_d = [torch.empty_like(delta) for _ in range(2)]
     s_in = torch.cuda.Stream(dev)
     s_out = torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(args.steps)]
-    ev_comp = [torch.cuda.Event() for _ in range(args.steps)]
-    ev_out = [torch.cuda.Event() for _ in range(args.steps)]
+    ev_in = [torch.cuda.Event() for _ in range(steps)]
+    ev_comp = [torch.cuda.Event() for _ in range(steps)]
+    ev_out = [torch.cuda.Event() for _ in range(steps)]
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -403,7 +465,7 @@ def run_gpu(args, w: gin.Workload, inp, world, rank, local):
     e_start.record(stream)
     s_in.wait_event(e_start)
     s_out.wait_event(e_start)
-    for i in range(args.steps):
+    for i in range(steps):
         bsel = i % 2
         with torch.cuda.stream(s_in):
             if i >= 2:
@@ -420,20 +482,23 @@ def run_gpu(args, w: gin.Workload, inp, world, rank, local):
             s_out.wait_event(ev_comp[i])
             out_h.copy_(o_d[bsel], non_blocking=True)
             ev_out[i].record(s_out)
-    stream.wait_event(ev_out[args.steps - 1])
+    stream.wait_event(ev_out[steps - 1])
     e_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
-    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / args.steps, world, dev)
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / steps, world, dev)
     h2d = x_h.numel() * x_h.element_size() + R_h.numel() * R_h.element_size()
     d2h = out_h.numel() * out_h.element_size()
     abi.attn_sync_status(ctx, stream)
     abi.attn_sync_status(ctx_alt, stream)
     abi.attn_destroy(ctx_alt)
     abi.attn_destroy(ctx)
+    del x_d, R_d, o_d, x, R, ck, cv, delta, wts
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
 
     if rank != 0:
-        return
+        return None
     peaks, peak_src = load_peaks()
     n = world
     if w.kind == "prefill":
@@ -471,8 +536,8 @@ def run_gpu(args, w: gin.Workload, inp, world, rank, local):
                           "same steps right after the timed one"}
     per_kernel = {k: {"ms_per_launch": v[0] / v[1], "launches": v[1], "share": v[0] / sum(x[0] for x in kinds.values())}
                   for k, v in kinds.items()}
-    line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": n, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+    return {"metric": METRIC, "value": value, "unit": unit, "n_gpus": n, "steps": steps,
+            "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) x, N(0,0.02) weights)",
             "config": workload_config(w), **extra, "roofline": roofline, "kernels": per_kernel,
             "gpu_launches": int(sum(v[1] for v in kinds.values())),
@@ -482,20 +547,54 @@ def run_gpu(args, w: gin.Workload, inp, world, rank, local):
                                 "double-buffered across steps; consecutive steps alternate two weight "
                                 "copies (168 MB > L2) instead of an L2 flush"},
             "clocks": clocks}
-    if n == 1 and not args.no_cpu_baseline:
+
+
+HEADLINE = "prefill_b1_t32768"
+SUB_WORKLOADS = ("prefill_b1_t16", "prefill_b1_t2048", "prefill_b4_t8192", "decode_b64_pos4095")
+# Short steps are timed over at least this many steps so that one record spans a few ms.
+MIN_SUB_STEPS = 100
+
+
+def run_gpu(args, w: gin.Workload, world, rank, local):
+    from transformer_gqa_attention_gb300 import _build
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    _build.build()
+    inp = gin.make_inputs(w)
+    line = measure_gpu(args, w, inp, world, rank, local, args.steps, args.warmup)
+    subs = {}
+    if not args.no_sub and w.name == HEADLINE:
+        for name in SUB_WORKLOADS:
+            sw = gin.WORKLOADS[name]
+            sinp = gin.make_inputs(sw)
+            steps = max(args.steps, MIN_SUB_STEPS) if (sw.kind == "decode" or sw.T <= 2048) else args.steps
+            subs[name] = measure_gpu(args, sw, sinp, world, rank, local, steps, args.warmup)
+            del sinp
+    if rank != 0:
+        return
+    if subs:
+        line["sub_records"] = subs
+    if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, w)
+        line["cpu_baseline"]["single_core"] = {name: single_core_baseline(name) for name in SINGLE_CORE_WORKLOADS}
     print(json.dumps(line))
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="prefill_b1_t2048", choices=sorted(gin.WORKLOADS))
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(gin.WORKLOADS))
     ap.add_argument("--impl", default="gqa", choices=["gqa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub", action="store_true", help="time only --workload (no sub-records)")
+    ap.add_argument("--oracle-one-core", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--one-core-budget", type=float, default=4.0, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_one_core:
+        _one_core_child(args.oracle_one_core, args.one_core_budget)
+        return
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_setup(args.gpus)
@@ -506,9 +605,8 @@ def main():
         return
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
-    inp = gin.make_inputs(w)
     try:
-        run_gpu(args, w, inp, world, rank, local)
+        run_gpu(args, w, world, rank, local)
     finally:
         if world > 1:
             torch.distributed.destroy_process_group()

@@ -230,18 +230,36 @@ gqa_status attn_profile_end(gqa_ctx *ctx, double *ms_per_kind, int *launches_per
  * Scratch: the per-split partial results live in one file-scope device array of about
  * 4.3 MB (2048 units of (sequence, kv head, key split)), which every GPU that loads this
  * library holds until the process exits.  The first call on a device looks up that
- * array's device address (cudaGetSymbolAddress) and configures the kernels; make that
- * first call before any stream capture.  Every call shares the array and it keeps the
- * last call's contents; calls whose work overlaps on the GPU (other streams or host
- * threads) race and must be serialised by the caller.  A device-side wait that runs out
- * is recorded in a status word inside the array, which each call clears first and which
- * this entry point does not report.
+ * array's device address (cudaGetSymbolAddress), the device's SM count and architecture,
+ * and configures the kernels; make that first call before any stream capture.  Every call
+ * shares the array and it keeps the last call's contents; calls whose work overlaps on the
+ * GPU (other streams or host threads) race and must be serialised by the caller.
+ * Time-outs: if a bounded device-side wait of this call runs out, every element of h is
+ * written as NaN (never a mix of stale partial results) and the time-out is recorded in a
+ * status word inside the array, which attn_decode_attention_noalloc_status reports.
  * Errors: GQA_ERR_INVALID_ARG, GQA_ERR_SHAPE, GQA_ERR_ALIGN, GQA_ERR_DEVICE (not sm_103),
- * GQA_ERR_CUDA.
+ * GQA_ERR_CUDA (the cause via attn_last_cuda_error).
  */
 gqa_status attn_decode_attention_noalloc(const void *q_r, const void *cache_k,
                                          const void *cache_v, int B, int kv_len, int S_max,
                                          void *h, gqa_stream_t stream);
+
+/*
+ * attn_decode_attention_noalloc_status — synchronise `stream`, then read and clear the
+ * status word of attn_decode_attention_noalloc on the current device (allocates nothing).
+ * Returns GQA_ERR_TIMEOUT if a device-side wait of any call since the last read ran out
+ * (those calls wrote NaN into their h), GQA_OK otherwise, or GQA_ERR_DEVICE / GQA_ERR_CUDA.
+ * The word is shared by every caller of the entry point on that device.
+ */
+gqa_status attn_decode_attention_noalloc_status(gqa_stream_t stream);
+
+/*
+ * attn_decode_attention_noalloc_debug_inject_timeout — test hook for that failure path (no
+ * counterpart on the pages): the next call of attn_decode_attention_noalloc (in any thread)
+ * makes its first work unit issue no loads, so that unit's bounded waits run out after about
+ * 2 s; nothing faults or hangs.  Always returns GQA_OK.
+ */
+gqa_status attn_decode_attention_noalloc_debug_inject_timeout(void);
 
 /*
  * attn_debug_inject_timeout — test hook for the failure path (no counterpart on the pages).

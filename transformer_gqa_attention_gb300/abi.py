@@ -21,6 +21,7 @@ EXPORTED = ("attn_create", "attn_prefill", "attn_decode", "attn_set_norm", "attn
             "attn_decode_residual", "attn_sync_status", "attn_debug_buffers",
             "attn_profile_begin", "attn_profile_end", "attn_debug_inject_timeout",
             "attn_debug_pair_schedule", "attn_decode_attention_noalloc",
+            "attn_decode_attention_noalloc_status", "attn_decode_attention_noalloc_debug_inject_timeout",
             "attn_destroy", "attn_strerror", "attn_last_cuda_error")
 
 # Kernel kinds of attn_profile_end (GQA_KERNEL_* in include/gqa_attn.h).
@@ -77,6 +78,10 @@ def lib() -> ctypes.CDLL:
     L.attn_debug_pair_schedule.restype = i32
     L.attn_decode_attention_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
     L.attn_decode_attention_noalloc.restype = i32
+    L.attn_decode_attention_noalloc_status.argtypes = [vp]
+    L.attn_decode_attention_noalloc_status.restype = i32
+    L.attn_decode_attention_noalloc_debug_inject_timeout.argtypes = []
+    L.attn_decode_attention_noalloc_debug_inject_timeout.restype = i32
     L.attn_destroy.argtypes = [vp]
     L.attn_destroy.restype = None
     L.attn_strerror.argtypes = [i32]
@@ -199,6 +204,18 @@ def attn_decode_attention_noalloc(q_r, cache_k, cache_v, B, kv_len, S_max, h, st
     _check("attn_decode_attention_noalloc",
            lib().attn_decode_attention_noalloc(_ptr(q_r), _ptr(cache_k), _ptr(cache_v), int(B),
                                                int(kv_len), int(S_max), _ptr(h), _stream(stream)))
+
+
+def attn_decode_attention_noalloc_status(stream=None):
+    """Synchronise the stream and raise GQAError(GQA_ERR_TIMEOUT) if a bounded wait of an
+    allocation-free call ran out since the last check (clears the status word)."""
+    _check("attn_decode_attention_noalloc_status", lib().attn_decode_attention_noalloc_status(_stream(stream)))
+
+
+def attn_decode_attention_noalloc_debug_inject_timeout():
+    """Arm the one-shot failure-path hook for the next allocation-free decode call."""
+    _check("attn_decode_attention_noalloc_debug_inject_timeout",
+           lib().attn_decode_attention_noalloc_debug_inject_timeout())
 
 
 def attn_destroy(ctx):

@@ -275,8 +275,22 @@ __global__ void __launch_bounds__(160)
 }
 
 // Separate merge kernel (used when the decode kernel runs without arrival counters).
-// grid (8, B), 128 threads.
+// grid (8, B), 128 threads, launched after decode_attn_kernel has completed.  If a split of
+// this call gave up a wait (*p.status non-zero), some partials were never written, so every
+// H entry of the call is written as NaN instead of a merge of stale partials, and the status
+// bits are OR-ed into *p.status_sticky, where they stay until the caller reads them.
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
+  const int st = *reinterpret_cast<volatile const int*>(p.status);
+  if (st != 0) {
+    const int hh = threadIdx.x >> 5;
+    const int d0 = (threadIdx.x & 31) * 4;
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.H) + static_cast<size_t>(blockIdx.y) * 4096 +
+                         (blockIdx.x * 4 + hh) * 128 + d0;
+    const uint32_t nan2 = 0x7FC07FC0u;  // two bf16 quiet NaNs
+    *reinterpret_cast<uint2*>(dst) = make_uint2(nan2, nan2);
+    if (p.status_sticky && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.status_sticky, st);
+    return;
+  }
   decode_merge_splits(p, blockIdx.y, blockIdx.x, threadIdx.x);
 }
 

@@ -44,11 +44,15 @@ struct gqa_ctx {
 };
 
 namespace {
-
 thread_local int g_last_cuda_error = 0;
+}  // namespace
+
+void gqa::set_last_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
+
+namespace {
 
 gqa_status cuda_fail(cudaError_t e) {
-  g_last_cuda_error = static_cast<int>(e);
+  set_last_cuda_error(e);
   return GQA_ERR_CUDA;
 }
 

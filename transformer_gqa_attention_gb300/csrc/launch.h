@@ -39,6 +39,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Records a failing CUDA call's error code for attn_last_cuda_error (thread-local; every
+// translation unit of the library reports through it).
+void set_last_cuda_error(cudaError_t e);
+
 // Dynamic shared memory each kernel needs (bytes).
 size_t gemm_wide_smem();    // 128x256 tiles (prefill)
 size_t gemm_skinny_smem();  // 128x64 tiles (few tokens, split-K)

@@ -63,6 +63,9 @@ struct DecodeParams {
   int* counters;           // [B*8] arrival counters: the last split merges (null: separate merge kernel)
   void* H;        // [B, 4096] bf16 (combine output)
   int* status;
+  // decode_combine_kernel only: when *status is non-zero (a split of this call gave up a
+  // wait), H is written as NaN and the status bits are OR-ed into *status_sticky (null: not)
+  int* status_sticky;
   int fault;      // test hook: CTA (0, 0, 0)'s producer issues no loads (its waits run out)
   float scale_log2;
 };
