@@ -80,6 +80,38 @@ gqa_status attn_create(const void *wq, const void *wk, const void *wv, const voi
                        gqa_stream_t stream, gqa_ctx **out);
 
 /*
+ * attn_create_shard — a context for one tensor-parallel shard of the block: the query heads
+ * of n_kv_local consecutive kv groups (4 n_kv_local query heads, n_kv_local key/value
+ * heads), as the quoted Attention.__init__ splits the block over model-parallel ranks
+ * (page "Llama 3.1 8B · Grouped-query attention", Query projection: n_local_heads =
+ * n_heads / model_parallel_size, n_local_kv_heads likewise; wq, wk, wv are
+ * ColumnParallelLinear(gather_output=False), whose weight is [output_size_per_partition,
+ * in_features]) and the output projection is a RowParallelLinear(input_is_parallel=True)
+ * whose weight is [out_features, input_size_per_partition] (page "Llama 3.1 8B · Merge and
+ * project").  Rank r of a world of w ranks holds kv groups 8r/w .. 8(r+1)/w - 1.
+ *
+ * wq_shard [512 n,4096]: rows 512 g0 .. 512 (g0+n) - 1 of W_Q (query heads 4 g0 .. 4 (g0+n) - 1)
+ * wk_shard, wv_shard [128 n,4096]: rows 128 g0 .. 128 (g0+n) - 1 of W_K, W_V
+ * wo_shard [4096,512 n]: columns 512 g0 .. 512 (g0+n) - 1 of W_O, row-major (densely packed)
+ * with n = n_kv_local in 1..8; all bf16 device tensors, copied into the context as by
+ * attn_create.
+ *
+ * attn_prefill / attn_decode on a shard context compute that shard's heads only:
+ *  - cache_k, cache_v are the shard's own caches [B,S_max,n,128] (its kv heads);
+ *  - attn_debug_buffers' q_r and h are [B*T,512 n];
+ *  - delta receives the shard's PARTIAL Delta_attn [B,T,4096] fp32 = H_shard W_O_shard^T:
+ *    the block's Delta_attn is the sum of the partials of all shards, which the row-parallel
+ *    output projection's all-reduce (a sum over ranks, done by the caller, e.g. with
+ *    torch.distributed.all_reduce) produces.
+ * The residual forms (attn_set_norm, attn_*_residual) need the whole sum and return
+ * GQA_ERR_INVALID_ARG on a shard context: apply attention_norm before the shards and add x
+ * after the all-reduce.  n_kv_local = 8 gives the same context as attn_create.
+ * Errors: those of attn_create, and GQA_ERR_SHAPE for n_kv_local outside 1..8.
+ */
+gqa_status attn_create_shard(const void *wq_shard, const void *wk_shard, const void *wv_shard,
+                             const void *wo_shard, int n_kv_local, gqa_stream_t stream, gqa_ctx **out);
+
+/*
  * attn_prefill — Delta_attn for T new positions of B sequences (steps 1-14).
  *
  * x       [B,T,4096] bf16: the block input, already normalised by the caller

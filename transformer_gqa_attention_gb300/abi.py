@@ -17,7 +17,7 @@ STATUS_NAMES = {0: "GQA_OK", 1: "GQA_ERR_INVALID_ARG", 2: "GQA_ERR_SHAPE", 3: "G
                 4: "GQA_ERR_CUDA", 5: "GQA_ERR_TIMEOUT", 6: "GQA_ERR_OOM", 7: "GQA_ERR_DEVICE"}
 
 # Every symbol include/gqa_attn.h declares.
-EXPORTED = ("attn_create", "attn_prefill", "attn_decode", "attn_set_norm", "attn_prefill_residual",
+EXPORTED = ("attn_create", "attn_create_shard", "attn_prefill", "attn_decode", "attn_set_norm", "attn_prefill_residual",
             "attn_decode_residual", "attn_sync_status", "attn_debug_buffers",
             "attn_profile_begin", "attn_profile_end", "attn_debug_inject_timeout",
             "attn_debug_pair_schedule", "attn_decode_attention_noalloc",
@@ -53,6 +53,8 @@ def lib() -> ctypes.CDLL:
     vp, i32 = ctypes.c_void_p, ctypes.c_int
     L.attn_create.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(vp)]
     L.attn_create.restype = i32
+    L.attn_create_shard.argtypes = [vp, vp, vp, vp, i32, vp, ctypes.POINTER(vp)]
+    L.attn_create_shard.restype = i32
     L.attn_prefill.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp, i32, i32, vp, vp]
     L.attn_prefill.restype = i32
     L.attn_decode.argtypes = [vp, vp, i32, i32, vp, vp, vp, i32, vp, vp]
@@ -118,6 +120,15 @@ def attn_create(wq, wk, wv, wo, stream=None) -> int:
     ctx = ctypes.c_void_p()
     _check("attn_create", lib().attn_create(_ptr(wq), _ptr(wk), _ptr(wv), _ptr(wo), _stream(stream),
                                             ctypes.byref(ctx)))
+    return ctx.value
+
+
+def attn_create_shard(wq_shard, wk_shard, wv_shard, wo_shard, n_kv_local, stream=None) -> int:
+    """Context for one tensor-parallel shard (n_kv_local kv groups; see tp.shard_weights)."""
+    ctx = ctypes.c_void_p()
+    _check("attn_create_shard", lib().attn_create_shard(_ptr(wq_shard), _ptr(wk_shard), _ptr(wv_shard),
+                                                        _ptr(wo_shard), int(n_kv_local), _stream(stream),
+                                                        ctypes.byref(ctx)))
     return ctx.value
 
 

@@ -3,7 +3,8 @@
 //
 // The 4 query heads of kv group g = h/4 share every key and value of that group
 // (K_G[h] = K_r[h/4], V_G[h] = V[h/4]), so one CTA serves (sequence b, group g, key
-// split) and streams each K/V byte of its split exactly once for all 4 heads.
+// split) and streams each K/V byte of its split exactly once for all 4 heads.  The number
+// of kv groups (8 for the whole block, fewer for a head shard) comes from the parameters.
 //
 //   warps 0..3  consumers: each takes 16 keys of every 64-key tile; S = q K^T and
 //               O += P V with mma.sync m16n8k16 (the 4 heads are rows 0..3 of the
@@ -41,7 +42,7 @@ __device__ __forceinline__ uint32_t dec_chunk_off(int key, int cd) {
 __device__ __forceinline__ void decode_merge_splits(const DecodeParams& p, int b, int g, int tid) {
   const int hh = tid >> 5;
   const int d0 = (tid & 31) * 4;
-  const size_t unit0 = (static_cast<size_t>(b) * 8 + g) * p.n_splits;
+  const size_t unit0 = (static_cast<size_t>(b) * p.n_kv + g) * p.n_splits;
   float M = -INFINITY;
   for (int s = 0; s < p.n_splits; ++s) M = fmaxf(M, __ldcg(p.part_ml + ((unit0 + s) * 4 + hh) * 2));
   const float Mu = (M == -INFINITY) ? 0.f : M;
@@ -57,7 +58,8 @@ __device__ __forceinline__ void decode_merge_splits(const DecodeParams& p, int b
     acc[3] += f * v.w;
   }
   const float inv = 1.f / Ls;
-  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.H) + static_cast<size_t>(b) * 4096 + (g * 4 + hh) * 128 + d0;
+  __nv_bfloat16* dst =
+      static_cast<__nv_bfloat16*>(p.H) + static_cast<size_t>(b) * (p.n_kv * 512) + (g * 4 + hh) * 128 + d0;
   uint2 w;
   w.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
   w.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
@@ -132,7 +134,8 @@ __global__ void __launch_bounds__(160)
     const int qc = (lane & 3) * 2;
     uint32_t qa[8][2];
     {
-      const uint32_t* qp = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.q) + static_cast<size_t>(b) * 4096 +
+      const uint32_t* qp = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                                             static_cast<size_t>(b) * (p.n_kv * 512) +
                                                              (g * 4 + (qrow & 3)) * 128);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
@@ -251,7 +254,7 @@ __global__ void __launch_bounds__(160)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[e] += f * red_o[(w * 4 + hh) * 128 + d0 + e];
       }
-      const size_t unit = (static_cast<size_t>(b) * 8 + g) * p.n_splits + split;
+      const size_t unit = (static_cast<size_t>(b) * p.n_kv + g) * p.n_splits + split;
       *reinterpret_cast<float4*>(p.part_o + (unit * 4 + hh) * 128 + d0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
       if ((tid & 31) == 0) {
         p.part_ml[(unit * 4 + hh) * 2 + 0] = M;
@@ -262,12 +265,12 @@ __global__ void __launch_bounds__(160)
         volatile int* last_flag = abort_flag + 1;
         __threadfence();
         asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (tid == 0) *last_flag = (atomicAdd(&p.counters[b * 8 + g], 1) == p.n_splits - 1);
+        if (tid == 0) *last_flag = (atomicAdd(&p.counters[b * p.n_kv + g], 1) == p.n_splits - 1);
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (*last_flag) {
           __threadfence();
           decode_merge_splits(p, b, g, tid);
-          if (tid == 0) p.counters[b * 8 + g] = 0;  // ready for the next call
+          if (tid == 0) p.counters[b * p.n_kv + g] = 0;  // ready for the next call
         }
       }
     }
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(160)
 }
 
 // Separate merge kernel (used when the decode kernel runs without arrival counters).
-// grid (8, B), 128 threads, launched after decode_attn_kernel has completed.  If a split of
+// grid (n_kv, B), 128 threads, launched after decode_attn_kernel has completed.  If a split of
 // this call gave up a wait (*p.status non-zero), some partials were never written, so every
 // H entry of the call is written as NaN instead of a merge of stale partials, and the status
 // bits are OR-ed into *p.status_sticky, where they stay until the caller reads them.
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
   if (st != 0) {
     const int hh = threadIdx.x >> 5;
     const int d0 = (threadIdx.x & 31) * 4;
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.H) + static_cast<size_t>(blockIdx.y) * 4096 +
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.H) + static_cast<size_t>(blockIdx.y) * (p.n_kv * 512) +
                          (blockIdx.x * 4 + hh) * 128 + d0;
     const uint32_t nan2 = 0x7FC07FC0u;  // two bf16 quiet NaNs
     *reinterpret_cast<uint2*>(dst) = make_uint2(nan2, nan2);

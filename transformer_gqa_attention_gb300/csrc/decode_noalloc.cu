@@ -161,6 +161,7 @@ extern "C" gqa_status attn_decode_attention_noalloc(const void* q_r, const void*
 
   DecodeParams p{};
   p.B = B;
+  p.n_kv = 8;
   p.kv_len = kv_len;
   p.n_splits = splits;
   p.tiles_per_split = tiles_per_split;

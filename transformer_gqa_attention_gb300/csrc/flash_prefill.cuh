@@ -1,6 +1,8 @@
 // flash_prefill.cuh — causal grouped-query attention for a prefill (steps 6-13 of
 // "Llama 3.1 8B · Grouped-query attention"): S = Q_r K_G^T, S / sqrt(128), + M, row
 // softmax, H = A V_G, written merged as [B*T, 4096] bf16 (head h at columns 128h..).
+// A context over G of the 8 kv groups has 4 G query heads: Q_r and H rows are 512 G wide
+// and the cache holds G kv heads per position; the kernel takes G from its parameters.
 //
 // One CTA = one sequence b, one 128-query tile and TWO query heads h0 = 2p, h1 = 2p+1 of
 // the same kv group g = h0/4 (K_G[h] = K_r[h/4], V_G[h] = V[h/4] is an index map: both
@@ -76,16 +78,16 @@ __global__ void __launch_bounds__(384, 1)
   const int w_in = static_cast<int>(blockIdx.x) - band * band_ctas;
   const int qi = w_in / (2 * p.groups_per_band);
   const int gp = w_in - qi * 2 * p.groups_per_band;
-  const int grp = band * p.groups_per_band + (gp >> 1);  // b * 8 + kv group
-  const int b = grp >> 3;
-  const int hp = ((grp & 7) << 1) | (gp & 1);
+  const int grp = band * p.groups_per_band + (gp >> 1);  // b * n_kv + kv group
+  const int b = grp / p.n_kv;
+  const int hp = ((grp - b * p.n_kv) << 1) | (gp & 1);
   const int h0 = 2 * hp;
   const int g = h0 >> 2;
   const int qt = p.n_qtiles - 1 - qi;  // heaviest tiles first
   const int q0 = qt * 128;
   const int kv_len = p.start_pos + p.T;
   const int kv_hi = p.causal ? min(kv_len, p.start_pos + q0 + 128) : kv_len;
-  const int n_kv = (kv_hi + 127) / 128;
+  const int n_ktiles = (kv_hi + 127) / 128;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 18; ++i) mbar_init(&bars[i], (i >= 11 && i <= 14) ? 128u : 1u);
@@ -121,7 +123,7 @@ __global__ void __launch_bounds__(384, 1)
         tma_load_3d(smem + L::kQ + i * L::kTile + L::kHalf, &tmQ, q_full, (h0 + i) * 128 + 64, q0, b);
       }
       int issued_k = 0, issued_v = 0;
-      for (int j = 0; j < (no_loads ? 0 : n_kv); ++j) {
+      for (int j = 0; j < (no_loads ? 0 : n_ktiles); ++j) {
         const int st = j & 1;
         const uint32_t ph = (j >> 1) & 1;
         if (!mbar_wait(&k_empty[st], ph ^ 1u, abort_flag, p.status)) break;
@@ -199,8 +201,8 @@ __global__ void __launch_bounds__(384, 1)
       issue_s(1, 0);
       commit(&k_empty[0]);
     }
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const bool more = j + 1 < n_kv;
+    for (int j = 0; ok && j < n_ktiles; ++j) {
+      const bool more = j + 1 < n_ktiles;
       // head slot 0: PV_0(j) in two halves as P arrives, then S_0(j+1)
       if (!(ok = wait(&v_full[j & 1], (j >> 1) & 1))) break;
       if (!(ok = wait(&p_lo[0], j & 1))) break;
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(384, 1)
     float m_used = -INFINITY;
     float l_sum = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
+    for (int j = 0; j < n_ktiles; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[slot], j & 1, abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();

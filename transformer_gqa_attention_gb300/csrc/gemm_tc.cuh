@@ -20,9 +20,11 @@
 // Epilogues:
 //   kQkvRope  — the fused Q/K/V projection (steps 1-5 of "Llama 3.1 8B · Grouped-query
 //               attention"): columns 0..4095 are Q, 4096..5119 K, 5120..6143 V of the
-//               packed [6144,4096] weight.  Q and K pairs (2j, 2j+1) are rotated by
-//               R[t, j] in fp32, then Q is stored to the Q_r buffer [B*T,4096] and K_r, V
-//               straight into the caches [B,S_max,8,128] at position start_pos + t.
+//               packed [6144,4096] weight (for a context over G of the 8 kv groups:
+//               512 G query, then 128 G key and 128 G value columns).  Q and K pairs
+//               (2j, 2j+1) are rotated by R[t, j] in fp32, then Q is stored to the Q_r
+//               buffer [B*T,512 G] and K_r, V straight into the caches [B,S_max,G,128] at
+//               position start_pos + t.
 //   kStoreF32 — Delta = H W_O^T (step 14) stored fp32 row-major.
 //   kSplitKQkv / kSplitKOut — the same two epilogues for the few-token kernel.
 #pragma once
@@ -90,12 +92,15 @@ __device__ __forceinline__ void load_rope(const GemmParams& p, const QkvRows& q,
   }
 }
 
-// Q/K/V epilogue of one staged chunk (columns col0 .. col0+31, all of one of Q, K, V).
+// Q/K/V epilogue of one staged chunk (columns col0 .. col0+31, all of one of Q, K, V: the
+// boundaries are multiples of 128).
 __device__ __forceinline__ void store_qkv_chunk(const GemmParams& p, const float* stage, int lane, const QkvRows& q,
                                                 int col0, const float4 (&cs)[4][2]) {
   const int cq = lane & 3;
   const int col = col0 + 8 * cq;
-  const bool is_v = col0 >= 5120;
+  const int k_col0 = p.q_cols;              // first key column
+  const int v_col0 = p.q_cols + p.kv_cols;  // first value column
+  const bool is_v = col0 >= v_col0;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int r = 8 * k + (lane >> 2);
@@ -117,11 +122,11 @@ __device__ __forceinline__ void store_qkv_chunk(const GemmParams& p, const float
                      pack_bf16x2(c1.z * x1.z - c1.w * x1.w, c1.w * x1.z + c1.z * x1.w));
     }
     __nv_bfloat16* dst;
-    if (col0 < 4096) {
-      dst = static_cast<__nv_bfloat16*>(p.out0) + static_cast<size_t>(q.m[k]) * 4096 + col;
+    if (col0 < k_col0) {
+      dst = static_cast<__nv_bfloat16*>(p.out0) + static_cast<size_t>(q.m[k]) * p.q_cols + col;
     } else {
       const size_t cache_row = static_cast<size_t>(q.b[k]) * p.S_max + p.start_pos + q.t[k];
-      dst = static_cast<__nv_bfloat16*>(is_v ? p.out2 : p.out1) + cache_row * 1024 + (col - (is_v ? 5120 : 4096));
+      dst = static_cast<__nv_bfloat16*>(is_v ? p.out2 : p.out1) + cache_row * p.kv_cols + (col - (is_v ? v_col0 : k_col0));
     }
     *reinterpret_cast<uint4*>(dst) = w;
   }
@@ -347,8 +352,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       // (one head slice) apart and so rotate by the same RoPE pairs, those of position
       // ((n0 / 32) + cp) mod 4 of a head slice.  Q/K items read all their rotation
       // coefficients before waiting for the accumulator, so the latency hides under the main
-      // loop.
-      const bool rope = EPI == kQkvRope && n0 < 5120;
+      // loop (an item may mix key and value chunks: each chunk picks its own store).
+      const bool rope = EPI == kQkvRope && n0 < p.q_cols + p.kv_cols;
       QkvRows qr{};
       float4 cs[4][4][2];
       // Delta items with a residual: the residual of chunk pair cp + 1 is read while pair cp
@@ -607,7 +612,7 @@ __global__ void __launch_bounds__(192, 1)
     const int ew = warp - 2;
     const int f0 = 4 * lane;
     const int m = m0 + f0;
-    const bool rope = EPI == kSplitKQkv && m < 5120;
+    const bool rope = EPI == kSplitKQkv && m < p.q_cols + p.kv_cols;
 #pragma unroll 2
     for (int tok = t_lo + ew; tok < t_hi; tok += 4) {
       float4 acc = *reinterpret_cast<const float4*>(red + tok * 128 + f0);
@@ -642,13 +647,14 @@ __global__ void __launch_bounds__(192, 1)
           acc = make_float4(cs.x * e0 - cs.y * o0, cs.y * e0 + cs.x * o0, cs.z * e1 - cs.w * o1, cs.w * e1 + cs.z * o1);
         }
         const uint2 o = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-        if (m < 4096) {
-          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.fin0) + static_cast<size_t>(tok) * 4096 + m) = o;
+        if (m < p.q_cols) {
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.fin0) + static_cast<size_t>(tok) * p.q_cols + m) = o;
         } else {
-          const bool is_v = m >= 5120;
+          const int v_col0 = p.q_cols + p.kv_cols;
+          const bool is_v = m >= v_col0;
           const size_t crow = static_cast<size_t>(b) * p.S_max + p.start_pos + t;
-          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(is_v ? p.fin2 : p.fin1) + crow * 1024 +
-                                    (m - (is_v ? 5120 : 4096))) = o;
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(is_v ? p.fin2 : p.fin1) + crow * p.kv_cols +
+                                    (m - (is_v ? v_col0 : p.q_cols))) = o;
         }
       }
     }

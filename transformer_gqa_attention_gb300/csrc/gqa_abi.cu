@@ -23,9 +23,15 @@ struct gqa_ctx {
   int device = -1;
   int num_sms = 0;
   int pair_clusters = 0;  // co-resident 2-CTA clusters of the pair GEMM
-  // weights, k-block-major: W_t[kb][row][64] for kb = 0..63
-  __nv_bfloat16* w_qkv = nullptr;  // 6144 rows: W_Q rows 0..4095, W_K 4096..5119, W_V 5120..6143
-  __nv_bfloat16* w_o = nullptr;    // 4096 rows
+  // kv groups of this context: 8 for the whole block, G < 8 for a head shard (4 G query
+  // heads); q_cols = 512 G query features, kv_cols = 128 G key (and value) features
+  int n_kv = 8;
+  int q_cols() const { return 512 * n_kv; }
+  int kv_cols() const { return 128 * n_kv; }
+  int qkv_rows() const { return 768 * n_kv; }
+  // weights, k-block-major: W_t[kb][row][64]
+  __nv_bfloat16* w_qkv = nullptr;  // qkv_rows x 4096: W_Q rows 0..q_cols-1, then W_K, then W_V
+  __nv_bfloat16* w_o = nullptr;    // 4096 rows x q_cols (the columns of W_O that belong to its heads)
   // residual form: W_QKV * diag(attention_norm weight), same layout (attn_set_norm)
   __nv_bfloat16* w_qkv_norm = nullptr;
   float norm_eps = 0.f;
@@ -110,40 +116,41 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, 
 }
 
 // GEMM operands are addressed as (column c < 64, row r, k block kb) with box 64 x box_rows x 1.
-// Row-major [rows, 4096] activation: element (c, r, kb) at r*8192 + kb*128 + 2c bytes.
-bool map_rows_k4096(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
-  const uint64_t dims[3] = {64, rows, 64};
-  const uint64_t strides[2] = {4096 * 2, 64 * 2};
+// Row-major [rows, k_cols] activation: element (c, r, kb) at r*2*k_cols + kb*128 + 2c bytes.
+bool map_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t k_cols, uint32_t box_rows) {
+  const uint64_t dims[3] = {64, rows, k_cols / 64};
+  const uint64_t strides[2] = {k_cols * 2, 64 * 2};
   const uint32_t box[3] = {64, box_rows, 1};
   return make_map(m, base, 3, dims, strides, box);
 }
 
-// k-block-major weight copy W_t[kb][row][64]: element (c, r, kb) at (kb*rows + r)*128 + 2c
-// bytes, so one box of consecutive rows is one contiguous read.
-bool map_weight_tiled(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
-  const uint64_t dims[3] = {64, rows, 64};
+// k-block-major weight copy W_t[kb][row][64] (kbs k blocks): element (c, r, kb) at
+// (kb*rows + r)*128 + 2c bytes, so one box of consecutive rows is one contiguous read.
+bool map_weight_tiled(CUtensorMap* m, const void* base, uint64_t rows, uint64_t kbs, uint32_t box_rows) {
+  const uint64_t dims[3] = {64, rows, kbs};
   const uint64_t strides[2] = {64 * 2, rows * 64 * 2};
   const uint32_t box[3] = {64, box_rows, 1};
   return make_map(m, base, 3, dims, strides, box);
 }
 
-// Copy a row-major [rows, 4096] bf16 weight into rows row0.. of a k-block-major copy with
-// total_rows rows (64 strided 2-D copies, at context creation only).
+// Copy a row-major [rows, 64 kbs] bf16 weight into rows row0.. of a k-block-major copy with
+// total_rows rows (kbs strided 2-D copies, at context creation only).
 cudaError_t copy_weight_tiled(void* dst, const void* src, size_t rows, size_t row0, size_t total_rows,
-                              cudaStream_t s) {
-  for (size_t kb = 0; kb < 64; ++kb) {
+                              size_t kbs, cudaStream_t s) {
+  for (size_t kb = 0; kb < kbs; ++kb) {
     uint8_t* d = static_cast<uint8_t*>(dst) + (kb * total_rows + row0) * 128;
     const uint8_t* from = static_cast<const uint8_t*>(src) + kb * 128;
-    cudaError_t e = cudaMemcpy2DAsync(d, 128, from, 8192, 128, rows, cudaMemcpyDeviceToDevice, s);
+    cudaError_t e = cudaMemcpy2DAsync(d, 128, from, kbs * 128, 128, rows, cudaMemcpyDeviceToDevice, s);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
-// KV cache [B, S_max, 8, 128] bf16 seen as (d, g, s < kv_len, b); box 64 d x key_rows.
-bool map_cache(CUtensorMap* m, const void* base, int B, int S_max, int kv_len, uint32_t key_rows) {
-  const uint64_t dims[4] = {128, 8, static_cast<uint64_t>(kv_len), static_cast<uint64_t>(B)};
-  const uint64_t strides[3] = {128 * 2, 1024 * 2, static_cast<uint64_t>(S_max) * 1024 * 2};
+// KV cache [B, S_max, n_kv, 128] bf16 seen as (d, g, s < kv_len, b); box 64 d x key_rows.
+bool map_cache(CUtensorMap* m, const void* base, int B, int S_max, int n_kv, int kv_len, uint32_t key_rows) {
+  const uint64_t dims[4] = {128, static_cast<uint64_t>(n_kv), static_cast<uint64_t>(kv_len), static_cast<uint64_t>(B)};
+  const uint64_t strides[3] = {128 * 2, static_cast<uint64_t>(n_kv) * 128 * 2,
+                               static_cast<uint64_t>(S_max) * n_kv * 128 * 2};
   const uint32_t box[4] = {64, 1, key_rows, 1};
   return make_map(m, base, 4, dims, strides, box);
 }
@@ -175,11 +182,11 @@ struct DecodePlan {
   int n_splits, tiles_per_split;
 };
 
-DecodePlan decode_plan(int B, int kv_len, int num_sms) {
+DecodePlan decode_plan(int B, int n_kv, int kv_len, int num_sms) {
   const int n_tiles = (kv_len + kDecTileKeys - 1) / kDecTileKeys;
   // aim for ~6-7 waves of two CTAs per SM, at least 4 tiles (256 keys) per split (B=64 at
   // 4096 keys: 4 splits of 16 tiles measured faster than 5, 8 or 10)
-  const long long units = static_cast<long long>(B) * 8;
+  const long long units = static_cast<long long>(B) * n_kv;
   const long long target = 13LL * num_sms;
   int splits = static_cast<int>(std::max(1LL, (target + units - 1) / units));
   splits = std::min(splits, std::max(1, n_tiles / 4));
@@ -189,17 +196,18 @@ DecodePlan decode_plan(int B, int kv_len, int num_sms) {
   return d;
 }
 
-WsLayout ws_layout(long long n_tok, const SkinnyPlan* sk, const DecodePlan* dp, int B_dec) {
+WsLayout ws_layout(long long n_tok, int n_kv, const SkinnyPlan* sk, const DecodePlan* dp, int B_dec) {
   WsLayout w{};
   size_t off = 0;
+  const size_t q_cols = static_cast<size_t>(n_kv) * 512;
   w.q_off = off;
-  off = round_up(off + static_cast<size_t>(n_tok) * 4096 * 2, 256);
+  off = round_up(off + static_cast<size_t>(n_tok) * q_cols * 2, 256);
   w.h_off = off;
-  off = round_up(off + static_cast<size_t>(n_tok) * 4096 * 2, 256);
+  off = round_up(off + static_cast<size_t>(n_tok) * q_cols * 2, 256);
   w.dec_o_off = off;
   w.dec_ml_off = off;
   if (dp) {
-    const size_t units = static_cast<size_t>(B_dec) * 8 * dp->n_splits;
+    const size_t units = static_cast<size_t>(B_dec) * n_kv * dp->n_splits;
     off = round_up(off + units * 4 * 128 * 4, 256);
     w.dec_ml_off = off;
     off = round_up(off + units * 4 * 2 * 4, 256);
@@ -284,15 +292,18 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
   p.start_pos = start_pos;
   p.status = c->status;
   p.num_kb = 64;
+  p.q_cols = c->q_cols();
+  p.kv_cols = c->kv_cols();
+  const int rows = c->qkv_rows();
   CUtensorMap ta, tb;
   if (sk) {
-    if (!map_weight_tiled(&ta, wqkv, 6144, 128) || !map_rows_k4096(&tb, x, n_tok, 64))
+    if (!map_weight_tiled(&ta, wqkv, rows, 64, 128) || !map_rows(&tb, x, n_tok, 4096, 64))
       return cuda_fail(cudaErrorInvalidValue);
-    p.M = 6144;
+    p.M = rows;
     p.N = n_tok;
     p.splits = sk->splits_qkv;
     p.n_tiles = sk->n_tiles;
-    p.m_tiles = 48;
+    p.m_tiles = rows / 128;
     p.fin0 = q_out;
     p.fin1 = ck;
     p.fin2 = cv;
@@ -302,12 +313,12 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
     { ProfScope ps(c, GQA_KERNEL_QKV_SPLITK, s); GQA_CUDA(launch_gemm_splitk_qkv(ta, tb, p, grid, s)); }
   } else {
     // CTA pairs, 256x256 tiles: each CTA loads 128-row boxes of x and of W_QKV
-    if (!map_rows_k4096(&ta, x, n_tok, 128) || !map_weight_tiled(&tb, wqkv, 6144, 128))
+    if (!map_rows(&ta, x, n_tok, 4096, 128) || !map_weight_tiled(&tb, wqkv, rows, 64, 128))
       return cuda_fail(cudaErrorInvalidValue);
     p.M = n_tok;
-    p.N = 6144;
+    p.N = rows;
     p.splits = 1;
-    p.n_tiles = 24;
+    p.n_tiles = rows / 256;
     p.m_tiles = (n_tok + 255) / 256;
     p.out0 = q_out;
     p.out1 = ck;
@@ -315,7 +326,7 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
     p.R = R;
     const int grid = plan_pair_grid(p, c->pair_clusters);
     CUtensorMap tbt = tb;  // boxes of tail_w / 2 rows for the pieces of a partial last round
-    if (p.tail_w && !map_weight_tiled(&tbt, wqkv, 6144, p.tail_w / 2)) return cuda_fail(cudaErrorInvalidValue);
+    if (p.tail_w && !map_weight_tiled(&tbt, wqkv, rows, 64, p.tail_w / 2)) return cuda_fail(cudaErrorInvalidValue);
     p.fault = take_fault(c, GQA_KERNEL_QKV_GEMM);
     { ProfScope ps(c, GQA_KERNEL_QKV_GEMM, s); GQA_CUDA(launch_gemm_qkv_rope(ta, tb, tbt, p, grid, s)); }
   }
@@ -328,10 +339,11 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
   GemmParams p{};
   p.residual = residual;  // residual form: x + Delta
   p.status = c->status;
-  p.num_kb = 64;
+  const int kc = c->q_cols();  // the contraction runs over this context's heads only
+  p.num_kb = kc / 64;
   CUtensorMap ta, tb;
   if (sk) {
-    if (!map_weight_tiled(&ta, c->w_o, 4096, 128) || !map_rows_k4096(&tb, h, n_tok, 64))
+    if (!map_weight_tiled(&ta, c->w_o, 4096, p.num_kb, 128) || !map_rows(&tb, h, n_tok, kc, 64))
       return cuda_fail(cudaErrorInvalidValue);
     p.M = 4096;
     p.N = n_tok;
@@ -343,7 +355,7 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
     p.fault = take_fault(c, GQA_KERNEL_OUT_SPLITK);
     { ProfScope ps(c, GQA_KERNEL_OUT_SPLITK, s); GQA_CUDA(launch_gemm_splitk_out(ta, tb, p, grid, s)); }
   } else {
-    if (!map_rows_k4096(&ta, h, n_tok, 128) || !map_weight_tiled(&tb, c->w_o, 4096, 128))
+    if (!map_rows(&ta, h, n_tok, kc, 128) || !map_weight_tiled(&tb, c->w_o, 4096, p.num_kb, 128))
       return cuda_fail(cudaErrorInvalidValue);
     p.M = n_tok;
     p.N = 4096;
@@ -354,7 +366,8 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
     p.ldo = 4096;
     const int grid = plan_pair_grid(p, c->pair_clusters);
     CUtensorMap tbt = tb;
-    if (p.tail_w && !map_weight_tiled(&tbt, c->w_o, 4096, p.tail_w / 2)) return cuda_fail(cudaErrorInvalidValue);
+    if (p.tail_w && !map_weight_tiled(&tbt, c->w_o, 4096, p.num_kb, p.tail_w / 2))
+      return cuda_fail(cudaErrorInvalidValue);
     p.fault = take_fault(c, GQA_KERNEL_OUT_GEMM);
     { ProfScope ps(c, GQA_KERNEL_OUT_GEMM, s); GQA_CUDA(launch_gemm_store_f32(ta, tb, tbt, p, grid, s)); }
   }
@@ -381,11 +394,18 @@ const char* attn_strerror(gqa_status st) {
 
 int attn_last_cuda_error(void) { return g_last_cuda_error; }
 
-gqa_status attn_create(const void* wq, const void* wk, const void* wv, const void* wo, gqa_stream_t stream,
-                       gqa_ctx** out) {
+}  // extern "C"
+
+namespace {
+
+// A context over n_kv kv groups (4 n_kv query heads) from row-major weights: wq [512 n_kv,
+// 4096], wk / wv [128 n_kv, 4096], wo [4096, 512 n_kv].
+gqa_status create_impl(const void* wq, const void* wk, const void* wv, const void* wo, int n_kv,
+                       cudaStream_t s, gqa_ctx** out) {
   if (!out) return GQA_ERR_INVALID_ARG;
   *out = nullptr;
   if (!wq || !wk || !wv || !wo) return GQA_ERR_INVALID_ARG;
+  if (n_kv < 1 || n_kv > 8) return GQA_ERR_SHAPE;
   if (!aligned16(wq) || !aligned16(wk) || !aligned16(wv) || !aligned16(wo)) return GQA_ERR_ALIGN;
   int dev = -1;
   GQA_CUDA(cudaGetDevice(&dev));
@@ -397,16 +417,16 @@ gqa_status attn_create(const void* wq, const void* wk, const void* wv, const voi
 
   gqa_ctx* c = new gqa_ctx();
   c->device = dev;
+  c->n_kv = n_kv;
   c->num_sms = prop.multiProcessorCount;
   c->pair_clusters = gemm_pair_max_clusters();
   if (c->pair_clusters <= 0) c->pair_clusters = prop.multiProcessorCount / 2;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   auto fail = [&](gqa_status st) {
     attn_destroy(c);
     return st;
   };
-  if (cudaMalloc(&c->w_qkv, size_t(6144) * 4096 * 2) != cudaSuccess ||
-      cudaMalloc(&c->w_o, size_t(4096) * 4096 * 2) != cudaSuccess ||
+  const size_t rows = c->qkv_rows(), qc = c->q_cols(), kvc = c->kv_cols();
+  if (cudaMalloc(&c->w_qkv, rows * 4096 * 2) != cudaSuccess || cudaMalloc(&c->w_o, 4096 * qc * 2) != cudaSuccess ||
       cudaMalloc(&c->status, sizeof(int)) != cudaSuccess ||
       cudaMalloc(&c->counters, kCounterInts * sizeof(int)) != cudaSuccess) {
     cudaGetLastError();
@@ -414,14 +434,29 @@ gqa_status attn_create(const void* wq, const void* wk, const void* wv, const voi
   }
   cudaError_t e = cudaMemsetAsync(c->status, 0, sizeof(int), s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->counters, 0, kCounterInts * sizeof(int), s);
-  // k-block-major copies: W_Q rows 0..4095, W_K 4096..5119, W_V 5120..6143 of W_QKV; W_O
-  if (e == cudaSuccess) e = copy_weight_tiled(c->w_qkv, wq, 4096, 0, 6144, s);
-  if (e == cudaSuccess) e = copy_weight_tiled(c->w_qkv, wk, 1024, 4096, 6144, s);
-  if (e == cudaSuccess) e = copy_weight_tiled(c->w_qkv, wv, 1024, 5120, 6144, s);
-  if (e == cudaSuccess) e = copy_weight_tiled(c->w_o, wo, 4096, 0, 4096, s);
+  // k-block-major copies: W_Q rows 0..qc-1, W_K qc..qc+kvc-1, W_V qc+kvc.. of W_QKV; W_O
+  if (e == cudaSuccess) e = copy_weight_tiled(c->w_qkv, wq, qc, 0, rows, 64, s);
+  if (e == cudaSuccess) e = copy_weight_tiled(c->w_qkv, wk, kvc, qc, rows, 64, s);
+  if (e == cudaSuccess) e = copy_weight_tiled(c->w_qkv, wv, kvc, qc + kvc, rows, 64, s);
+  if (e == cudaSuccess) e = copy_weight_tiled(c->w_o, wo, 4096, 0, 4096, qc / 64, s);
   if (e != cudaSuccess) return fail(cuda_fail(e));
   *out = c;
   return GQA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gqa_status attn_create(const void* wq, const void* wk, const void* wv, const void* wo, gqa_stream_t stream,
+                       gqa_ctx** out) {
+  return create_impl(wq, wk, wv, wo, 8, reinterpret_cast<cudaStream_t>(stream), out);
+}
+
+gqa_status attn_create_shard(const void* wq_shard, const void* wk_shard, const void* wv_shard, const void* wo_shard,
+                             int n_kv_local, gqa_stream_t stream, gqa_ctx** out) {
+  return create_impl(wq_shard, wk_shard, wv_shard, wo_shard, n_kv_local, reinterpret_cast<cudaStream_t>(stream),
+                     out);
 }
 
 }  // extern "C"
@@ -445,14 +480,15 @@ gqa_status prefill_impl(gqa_ctx* c, const void* x, int B, int T, const float* R,
   if (static_cast<long long>(B) * T > kMaxTokens) return GQA_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(R) || !aligned16(cache_k) || !aligned16(cache_v) || !aligned16(delta))
     return GQA_ERR_ALIGN;
-  if (residual && !c->w_qkv_norm) return GQA_ERR_INVALID_ARG;  // attn_set_norm not called
+  if (residual && !c->w_qkv_norm) return GQA_ERR_INVALID_ARG;  // attn_set_norm not called (never on a shard)
   gqa_status st = check_device(c);
   if (st != GQA_OK) return st;
 
   const int n_tok = B * T;
+  const int G = c->n_kv;
   SkinnyPlan sk_v = skinny_plan(n_tok, c->num_sms);
   const SkinnyPlan* sk = n_tok <= kSkinnyMaxTokens ? &sk_v : nullptr;
-  const WsLayout w = ws_layout(n_tok, sk, nullptr, 0);
+  const WsLayout w = ws_layout(n_tok, G, sk, nullptr, 0);
   st = ensure_ws(c, w.total, s);
   if (st != GQA_OK) return st;
   void* q_r = c->ws + w.q_off;
@@ -472,13 +508,14 @@ gqa_status prefill_impl(gqa_ctx* c, const void* x, int B, int T, const float* R,
   const int kv_len = start_pos + T;
   CUtensorMap tq, tk, tv, th;
   {
-    // Q_r (read) and H (written) are both [B, T, 4096] bf16, addressed in 64 x 128 boxes
-    const uint64_t dims[3] = {4096, static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
-    const uint64_t strides[2] = {4096 * 2, static_cast<uint64_t>(T) * 4096 * 2};
+    // Q_r (read) and H (written) are both [B, T, 512 G] bf16, addressed in 64 x 128 boxes
+    const uint64_t qc = c->q_cols();
+    const uint64_t dims[3] = {qc, static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
+    const uint64_t strides[2] = {qc * 2, static_cast<uint64_t>(T) * qc * 2};
     const uint32_t box[3] = {64, 128, 1};
     if (!make_map(&tq, q_r, 3, dims, strides, box) || !make_map(&th, h, 3, dims, strides, box) ||
-        !map_cache(&tk, cache_k, B, S_max, kv_len, 128) ||
-        !map_cache(&tv, cache_v, B, S_max, kv_len, 128))
+        !map_cache(&tk, cache_k, B, S_max, G, kv_len, 128) ||
+        !map_cache(&tv, cache_v, B, S_max, G, kv_len, 128))
       return cuda_fail(cudaErrorInvalidValue);
   }
   FlashParams fp{};
@@ -487,23 +524,25 @@ gqa_status prefill_impl(gqa_ctx* c, const void* x, int B, int T, const float* R,
   fp.S_max = S_max;
   fp.start_pos = start_pos;
   fp.causal = causal ? 1 : 0;
+  fp.n_kv = G;
   fp.n_qtiles = (T + 127) / 128;
   fp.status = c->status;
   fp.scale_log2 = kScaleLog2;
   fp.fault = take_fault(c, GQA_KERNEL_FLASH_PREFILL);
   // Scheduling bands: all (sequence, kv group) pairs at once while their K/V (kv_len x 512 B
-  // each) total at most 64 MB; otherwise the largest power-of-two count of pairs dividing 8
-  // whose K/V fit in 32 MB, so the CTAs resident together reuse K/V tiles through L2.
+  // each) total at most 64 MB; otherwise the largest count of one sequence's G groups, halved
+  // while it divides G, whose K/V fit in 32 MB, so the CTAs resident together reuse K/V tiles
+  // through L2.
   {
     const long long kv_bytes = static_cast<long long>(kv_len) * 512;
-    int gpb = 8 * B;
+    int gpb = G * B;
     if (kv_bytes * gpb > (64LL << 20)) {
-      gpb = 8;
-      while (gpb > 1 && kv_bytes * gpb > (32LL << 20)) gpb >>= 1;
+      gpb = G;
+      while (gpb > 1 && (gpb & 1) == 0 && kv_bytes * gpb > (32LL << 20)) gpb >>= 1;
     }
     fp.groups_per_band = gpb;
   }
-  { ProfScope ps(c, GQA_KERNEL_FLASH_PREFILL, s); GQA_CUDA(launch_flash_prefill(tq, tk, tv, th, fp, dim3(B * 16 * fp.n_qtiles), s)); }
+  { ProfScope ps(c, GQA_KERNEL_FLASH_PREFILL, s); GQA_CUDA(launch_flash_prefill(tq, tk, tv, th, fp, dim3(B * 2 * G * fp.n_qtiles), s)); }
 
   return run_out(c, h, n_tok, delta, w, sk, residual ? x : nullptr, s);
 }
@@ -515,15 +554,16 @@ gqa_status decode_impl(gqa_ctx* c, const void* x, int B, int start_pos, const fl
     return GQA_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(R_row) || !aligned16(cache_k) || !aligned16(cache_v) || !aligned16(delta))
     return GQA_ERR_ALIGN;
-  if (residual && !c->w_qkv_norm) return GQA_ERR_INVALID_ARG;  // attn_set_norm not called
+  if (residual && !c->w_qkv_norm) return GQA_ERR_INVALID_ARG;  // attn_set_norm not called (never on a shard)
   gqa_status st = check_device(c);
   if (st != GQA_OK) return st;
 
   const int kv_len = start_pos + 1;
+  const int G = c->n_kv;
   SkinnyPlan sk_v = skinny_plan(B, c->num_sms);
   const SkinnyPlan* sk = B <= kSkinnyMaxTokens ? &sk_v : nullptr;
-  const DecodePlan dp = decode_plan(B, kv_len, c->num_sms);
-  const WsLayout w = ws_layout(B, sk, &dp, B);
+  const DecodePlan dp = decode_plan(B, G, kv_len, c->num_sms);
+  const WsLayout w = ws_layout(B, G, sk, &dp, B);
   st = ensure_ws(c, w.total, s);
   if (st != GQA_OK) return st;
   void* q_r = c->ws + w.q_off;
@@ -542,11 +582,12 @@ gqa_status decode_impl(gqa_ctx* c, const void* x, int B, int start_pos, const fl
 
   // steps 6-13 against the cache (no mask: every key 0..start_pos is visible)
   CUtensorMap tk, tv;
-  if (!map_cache(&tk, cache_k, B, S_max, kv_len, kDecTileKeys) ||
-      !map_cache(&tv, cache_v, B, S_max, kv_len, kDecTileKeys))
+  if (!map_cache(&tk, cache_k, B, S_max, G, kv_len, kDecTileKeys) ||
+      !map_cache(&tv, cache_v, B, S_max, G, kv_len, kDecTileKeys))
     return cuda_fail(cudaErrorInvalidValue);
   DecodeParams p{};
   p.B = B;
+  p.n_kv = G;
   p.kv_len = kv_len;
   p.n_splits = dp.n_splits;
   p.tiles_per_split = dp.tiles_per_split;
@@ -558,7 +599,7 @@ gqa_status decode_impl(gqa_ctx* c, const void* x, int B, int start_pos, const fl
   p.scale_log2 = kScaleLog2;
   p.counters = c->counters;  // the last split of each (b, g) merges
   p.fault = take_fault(c, GQA_KERNEL_DECODE_ATTN);
-  { ProfScope ps(c, GQA_KERNEL_DECODE_ATTN, s); GQA_CUDA(launch_decode_attn(tk, tv, p, dim3(dp.n_splits, 8, B), s)); }
+  { ProfScope ps(c, GQA_KERNEL_DECODE_ATTN, s); GQA_CUDA(launch_decode_attn(tk, tv, p, dim3(dp.n_splits, G, B), s)); }
 
   // step 14
   return run_out(c, h, B, delta, w, sk, residual ? x : nullptr, s);
@@ -596,6 +637,8 @@ gqa_status attn_decode_residual(gqa_ctx* c, const void* x, int B, int start_pos,
 gqa_status attn_set_norm(gqa_ctx* c, const void* norm_w, float eps, gqa_stream_t stream) {
   if (!c || !norm_w || !(eps > 0.f) || !std::isfinite(eps)) return GQA_ERR_INVALID_ARG;
   if (!aligned16(norm_w)) return GQA_ERR_ALIGN;
+  // the residual form adds x once, after the whole sum over heads: not on a head shard
+  if (c->n_kv != 8) return GQA_ERR_INVALID_ARG;
   gqa_status st = check_device(c);
   if (st != GQA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

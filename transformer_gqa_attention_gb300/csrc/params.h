@@ -26,14 +26,18 @@ struct GemmParams {
   // CTA-pair kernel schedule: full_rounds rounds of whole 256x256 tiles, then the tiles of
   // the last, partial round cut into pieces of tail_w columns (0: whole tiles throughout)
   int full_rounds, tail_w;
+  // Q/K/V epilogues: the packed weight's rows are q_cols query features (4 heads x 128 per
+  // kv group), then kv_cols key and kv_cols value features (128 per kv group); Q_r rows are
+  // q_cols wide and a cache position holds kv_cols features.  The whole block: 4096 / 1024.
+  int q_cols, kv_cols;
   // epilogue operands
-  void* out0;        // kQkvRope: Q_r [M,4096] bf16 | kStoreF32: D fp32
+  void* out0;        // kQkvRope: Q_r [M,q_cols] bf16 | kStoreF32: D fp32
   void* out1;        // kQkvRope: cache_k
   void* out2;        // kQkvRope: cache_v
   const float* R;    // Q/K/V epilogues: [T,64,2]
   int T, S_max, start_pos;
   int ldo;           // kStoreF32: row stride (floats)
-  void* fin0;        // split-K final outputs: Q_r [N,4096] bf16 | Delta [N,4096] fp32
+  void* fin0;        // split-K final outputs: Q_r [N,q_cols] bf16 | Delta [N,4096] fp32
   void* fin1;        // kSplitKQkv: cache_k
   void* fin2;        // kSplitKQkv: cache_v
   int* status;
@@ -45,8 +49,9 @@ struct GemmParams {
 
 struct FlashParams {
   int B, T, S_max, start_pos, causal;
+  int n_kv;             // kv groups (heads of K/V) of the context; 4 query heads each
   int n_qtiles;
-  int groups_per_band;  // (sequence, kv group) pairs scheduled together (divides 8 B)
+  int groups_per_band;  // (sequence, kv group) pairs scheduled together (divides n_kv B)
   int* status;
   int fault;  // test hook: CTA 0's producer issues no loads (its waits run out)
   float scale_log2;  // log2(e) / sqrt(128)
@@ -57,11 +62,12 @@ constexpr int kDecTileKeys = 64;
 
 struct DecodeParams {
   int B, kv_len, n_splits, tiles_per_split;
-  const void* q;  // [B, 4096] bf16 rotated queries
-  float* part_o;           // [B, 8, n_splits, 4, 128]
-  float* part_ml;          // [B, 8, n_splits, 4, 2]
-  int* counters;           // [B*8] arrival counters: the last split merges (null: separate merge kernel)
-  void* H;        // [B, 4096] bf16 (combine output)
+  int n_kv;       // kv groups of the context (4 query heads each; q and H rows are 512 n_kv wide)
+  const void* q;  // [B, 512 n_kv] bf16 rotated queries
+  float* part_o;           // [B, n_kv, n_splits, 4, 128]
+  float* part_ml;          // [B, n_kv, n_splits, 4, 2]
+  int* counters;           // [B*n_kv] arrival counters: the last split merges (null: separate merge kernel)
+  void* H;        // [B, 512 n_kv] bf16 (combine output)
   int* status;
   // decode_combine_kernel only: when *status is non-zero (a split of this call gave up a
   // wait), H is written as NaN and the status bits are OR-ed into *status_sticky (null: not)
