@@ -322,6 +322,15 @@ gqa_status attn_debug_pair_schedule(int m_tiles, int n_tiles, int n_pairs, int *
                                     int *tail_w, int *grid_ctas, int *items, int max_items,
                                     int *n_items);
 
+/*
+ * attn_debug_exp2 — the two exponentials the prefill softmax uses, on n fp32 device inputs a
+ * (no counterpart on the pages; for tests): out_fma[i] = 2^a[i] by the FMA-pipe cubic
+ * (range reduction, a minimax cubic fitted for relative error, exponent insertion; inputs
+ * below -125 give 2^-125) and out_mufu[i] = ex2.approx.ftz(a[i]), both fp32 device arrays of
+ * n elements.  Enqueued on `stream`.  Errors: GQA_ERR_INVALID_ARG (null, n < 1), GQA_ERR_CUDA.
+ */
+gqa_status attn_debug_exp2(const float *a, float *out_fma, float *out_mufu, int n, gqa_stream_t stream);
+
 /* attn_destroy — free everything the context owns (after synchronising the device).
  * NULL is ignored. */
 void attn_destroy(gqa_ctx *ctx);

@@ -21,7 +21,7 @@ def L():
 def declared_functions():
     src = open(os.path.join(ROOT, "include", "gqa_attn.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_declares_the_boundary():
@@ -146,3 +146,19 @@ def test_set_norm_validation(L):
     assert abi.raw_status("attn_set_norm", vp(FAKE), vp(FAKE), f(float("nan")), None) == 1
     assert abi.raw_status("attn_set_norm", vp(FAKE), vp(FAKE), f(float("inf")), None) == 1
     assert abi.raw_status("attn_set_norm", vp(FAKE), vp(FAKE + 2), f(1e-5), None) == 3
+
+
+def test_create_shard_validation(L):
+    out = vp()
+    assert abi.raw_status("attn_create_shard", None, vp(FAKE), vp(FAKE), vp(FAKE), 4, None, ctypes.byref(out)) == 1
+    for n in (0, 9, -1):
+        assert abi.raw_status("attn_create_shard", vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), n, None,
+                              ctypes.byref(out)) == 2
+    assert abi.raw_status("attn_create_shard", vp(FAKE), vp(FAKE), vp(FAKE + 8), vp(FAKE), 2, None,
+                          ctypes.byref(out)) == 3
+    assert out.value is None
+
+
+def test_debug_exp2_validation(L):
+    assert abi.raw_status("attn_debug_exp2", None, vp(FAKE), vp(FAKE), 4, None) == 1
+    assert abi.raw_status("attn_debug_exp2", vp(FAKE), vp(FAKE), vp(FAKE), 0, None) == 1

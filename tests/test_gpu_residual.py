@@ -15,11 +15,14 @@ pytestmark = pytest.mark.gpu
 
 EPS = 1e-5
 
-# The update h - x carries one bf16 rounding more than the block alone: attention_norm's weight
-# is folded into the projection weights, W diag(w) rounded to bf16 (the quoted model takes the
-# same extra rounding where it stores attention_norm(x) in bf16 before the projections).  On
-# top of the block's floor (~4.1e-3 rel-L1 from the bf16 Q_r, K_r, V, P and H) that rounding
-# adds ~1e-3; the bound keeps headroom for it.  h itself is held to the block's 5e-3.
+# The update h - x carries one bf16 rounding more than the block alone: a bf16 GEMM needs either
+# attention_norm(x) or the weights in bf16, and the library folds the norm weight into the
+# projection weights, W diag(w) rounded to bf16.  An fp64 emulation of exactly the GPU's
+# roundings (tests/test_residual_floor.py) puts the update's floor at ~5.3e-3 rel-L1 for
+# T <= 300 and 5.75e-3 on the T = 2048 workload (the block alone: 4.0e-3 / 4.35e-3); rounding the
+# normalised activation once instead gives the same floor, rounding it twice as the quoted
+# RMSNorm does gives ~6.8e-3.  The bound is ~1.2 x the largest floor, the block's own margin.
+# h itself is held to the block's 5e-3.
 TOL_UPDATE_REL_L1 = 7e-3
 
 

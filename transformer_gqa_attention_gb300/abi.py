@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "GQA_OK", 1: "GQA_ERR_INVALID_ARG", 2: "GQA_ERR_SHAPE", 3: "G
 EXPORTED = ("attn_create", "attn_create_shard", "attn_prefill", "attn_decode", "attn_set_norm", "attn_prefill_residual",
             "attn_decode_residual", "attn_sync_status", "attn_debug_buffers",
             "attn_profile_begin", "attn_profile_end", "attn_debug_inject_timeout",
-            "attn_debug_pair_schedule", "attn_decode_attention_noalloc",
+            "attn_debug_pair_schedule", "attn_debug_exp2", "attn_decode_attention_noalloc",
             "attn_decode_attention_noalloc_status", "attn_decode_attention_noalloc_debug_inject_timeout",
             "attn_destroy", "attn_strerror", "attn_last_cuda_error")
 
@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
     ip = ctypes.POINTER(i32)
     L.attn_debug_pair_schedule.argtypes = [i32, i32, i32, ip, ip, ip, ip, i32, ip]
     L.attn_debug_pair_schedule.restype = i32
+    L.attn_debug_exp2.argtypes = [vp, vp, vp, i32, vp]
+    L.attn_debug_exp2.restype = i32
     L.attn_decode_attention_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
     L.attn_decode_attention_noalloc.restype = i32
     L.attn_decode_attention_noalloc_status.argtypes = [vp]
@@ -200,6 +202,13 @@ def attn_debug_pair_schedule(m_tiles, n_tiles, n_pairs):
                                       ctypes.byref(grid), buf, n.value, ctypes.byref(n)))
     items = [tuple(buf[4 * i:4 * i + 4]) for i in range(n.value)]
     return full.value, tail.value, grid.value, items
+
+
+def attn_debug_exp2(a, out_fma, out_mufu, stream=None):
+    """Evaluate the softmax's two exponentials (FMA-pipe cubic, ex2.approx) on a fp32 device
+    tensor into two fp32 device tensors of the same size."""
+    _check("attn_debug_exp2", lib().attn_debug_exp2(_ptr(a), _ptr(out_fma), _ptr(out_mufu), int(a.numel()),
+                                                    _stream(stream)))
 
 
 def attn_debug_inject_timeout(ctx, kind):

@@ -29,10 +29,22 @@
 // TMEM columns: S_0/P_0 at 0, S_1/P_1 at 128, O_0 at 256, O_1 at 384 (512 allocated).
 #pragma once
 
+#include <type_traits>
+
 #include "params.h"
 #include "ptx.cuh"
 
 namespace gqa {
+
+// Pairs of every 16 in a softmax chunk whose exponentials run on the FMA pipe (exp2_fma2)
+// instead of the multi-function unit.  Measured on GB300 with 0, 2, 4, 6 and 8 of 16: every
+// share made the kernel slower (B=1 x T=32768: 5.06-5.13 ms at 0, 5.16 at 2, 5.26-5.33 at 4,
+// 5.74 at 8), so the softmax phase is not bounded by the multi-function unit here and the
+// default is 0; the cubic stays available for parts where it is.
+#ifndef GQA_FLASH_FMA_EXP2_PAIRS
+#define GQA_FLASH_FMA_EXP2_PAIRS 0
+#endif
+constexpr int kFmaExp2Pairs = GQA_FLASH_FMA_EXP2_PAIRS;
 
 struct FlashSmem {
   static constexpr int kTile = 128 * 128 * 2;  // one 128x128 bf16 tile (two 64-column halves)
@@ -295,18 +307,37 @@ __global__ void __launch_bounds__(384, 1)
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
       const float2 nmu2 = make_float2(-mu, -mu);
       float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      // Chunk c (keys 32c .. 32c+31) as 16 pairs.  On key tiles without masked entries the
+      // last kFmaExp2Pairs pairs of each chunk take their exponentials on the FMA pipe
+      // (exp2_fma2), the others on the multi-function unit, which alone would bound this
+      // phase; tiles with masked (-inf) entries use the multi-function unit throughout, so
+      // masked probabilities stay exactly 0.
+      auto exp_chunk = [&](auto use_fma, int c, uint32_t(&w)[16]) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float2 a = ffma2(make_float2(__uint_as_float(sv[c * 32 + 2 * e]), __uint_as_float(sv[c * 32 + 2 * e + 1])),
+                                 sc2, nmu2);
+          float2 pe;
+          if (decltype(use_fma)::value && e >= 16 - kFmaExp2Pairs)
+            pe = exp2_fma2(a);
+          else
+            pe = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+          l4[e & 3] = fadd2(l4[e & 3], pe);
+          w[e] = pack_bf16x2(pe.x, pe.y);
+        }
+      };
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
         for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
           uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float2 a = ffma2(make_float2(__uint_as_float(sv[c * 32 + 2 * e]), __uint_as_float(sv[c * 32 + 2 * e + 1])),
-                                   sc2, nmu2);
-            const float2 pe = make_float2(fast_exp2(a.x), fast_exp2(a.y));
-            l4[e & 3] = fadd2(l4[e & 3], pe);
-            w[e] = pack_bf16x2(pe.x, pe.y);
+          if constexpr (kFmaExp2Pairs > 0) {
+            if (needs_mask)
+              exp_chunk(std::false_type{}, c, w);
+            else
+              exp_chunk(std::true_type{}, c, w);
+          } else {
+            exp_chunk(std::false_type{}, c, w);
           }
           tmem_st16(t_s + c * 16, w);
         }

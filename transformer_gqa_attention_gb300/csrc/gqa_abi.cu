@@ -718,6 +718,12 @@ gqa_status attn_debug_pair_schedule(int m_tiles, int n_tiles, int n_pairs, int* 
   return n > max_items ? GQA_ERR_SHAPE : GQA_OK;
 }
 
+gqa_status attn_debug_exp2(const float* a, float* out_fma, float* out_mufu, int n, gqa_stream_t stream) {
+  if (!a || !out_fma || !out_mufu || n < 1) return GQA_ERR_INVALID_ARG;
+  GQA_CUDA(launch_exp2_compare(a, out_fma, out_mufu, n, reinterpret_cast<cudaStream_t>(stream)));
+  return GQA_OK;
+}
+
 gqa_status attn_profile_begin(gqa_ctx* c) {
   if (!c) return GQA_ERR_INVALID_ARG;
   c->profiling = true;

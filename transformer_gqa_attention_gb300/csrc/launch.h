@@ -72,6 +72,7 @@ cudaError_t launch_flash_prefill(const CUtensorMap& q, const CUtensorMap& k, con
 cudaError_t launch_decode_attn(const CUtensorMap& k, const CUtensorMap& v, const DecodeParams& p,
                                dim3 grid, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeParams& p, int B, cudaStream_t s);
+cudaError_t launch_exp2_compare(const float* a, float* out_fma, float* out_mufu, int n, cudaStream_t s);
 cudaError_t launch_rms_rstd(const void* x, int rows, float eps, float* r, cudaStream_t s);
 cudaError_t launch_fold_norm_weight(const void* src, const void* w, int rows, void* dst, cudaStream_t s);
 

@@ -557,4 +557,33 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
   return d;
 }
 
+// 2^a for a pair of fp32 values on the FMA pipe instead of the multi-function unit: additive
+// range reduction a = j + f (j = rint(a) from the fp32 add of 1.5 * 2^23, f in [-1/2, 1/2]),
+// a cubic p(f) ~ 2^f, and j added to p's exponent field.  The cubic's coefficients are the
+// fp32-rounded minimax fit in relative error over [-1/2, 1/2] (Remez exchange), made by
+// csrc/fit_exp2_poly.py; relative error of the whole evaluation <= 7.5e-5 for a in [-125, 8].
+// Inputs below -125 are clamped to -125 (result 2^-125, not 0): callers pass finite values
+// whose exponentials that small do not matter next to their row sum (>= 1).
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 exp2_fma2(float2 a) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  constexpr float c0 = 0x1.fff692p-1f, c1 = 0x1.62f31ap-1f, c2 = 0x1.f0de1ap-3f, c3 = 0x1.c3f76p-5f;
+  a = make_float2(fmaxf(a.x, -125.f), fmaxf(a.y, -125.f));
+  const float2 t = fadd2(a, make_float2(kRound, kRound));   // j in the low mantissa bits
+  const float2 f = fsub2(a, fsub2(t, make_float2(kRound, kRound)));
+  float2 p = ffma2(make_float2(c3, c3), f, make_float2(c2, c2));
+  p = ffma2(p, f, make_float2(c1, c1));
+  p = ffma2(p, f, make_float2(c0, c0));
+  return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
+                     __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
+}
+
 }  // namespace gqa
