@@ -96,9 +96,12 @@ def load_peaks():
 
 
 def source_digest():
+    """Digest of the CUDA/C++ sources of the library (the kernels the ncu figures describe)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "transformer_gqa_attention_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
+        if not f.endswith((".cu", ".cuh", ".h")):
+            continue
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())

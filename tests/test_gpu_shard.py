@@ -125,3 +125,44 @@ def test_residual_form_is_rejected_on_a_shard():
         assert abi.raw_status("attn_set_norm", sh.ctx, w.data_ptr(), ctypes.c_float(1e-5), None) == 1
     finally:
         sh.close()
+
+
+def test_shard_chunked_prefill_and_large_decode_batch():
+    # a 2-way split: each shard prefills 150 positions, then continues with 100 more at
+    # start_pos = 150 against its own cache; then a decode of 80 sequences (more than 64
+    # tokens: the many-token projection kernels) on a filled cache
+    B, T1, T2 = 2, 150, 100
+    inp = gin.make_custom(seed=99, B=B, T=T1 + T2)
+    w64 = [gin.to_f64(t) for t in (inp.wq, inp.wk, inp.wv, inp.wo)]
+    ref, _ = orc.attention_block(gin.to_f64(inp.x), *w64, gin.to_f64(inp.R))
+    Bd, pos, S_d = 80, 300, 320
+    dec = gin.make_custom(seed=100, B=Bd, T=1, start_pos=pos, S_max=S_d, fill_cache=True)
+    wd64 = [gin.to_f64(t) for t in (dec.wq, dec.wk, dec.wv, dec.wo)]
+    ref_d, _ = orc.attention_decode(gin.to_f64(dec.x), *wd64, gin.to_f64(dec.R), gin.to_f64(dec.cache_k),
+                                    gin.to_f64(dec.cache_v), pos)
+    total = np.zeros(ref.shape)
+    total_d = np.zeros(ref_d.shape)
+    for g0, n in _splits(2):
+        sh = Shard(inp, g0, n)
+        try:
+            ck, cv = _shard_cache(B, T1 + T2, n)
+            for t0, t1 in ((0, T1), (T1, T1 + T2)):
+                d = torch.empty(B, t1 - t0, 4096, dtype=torch.float32, device=gu.DEV)
+                abi.attn_prefill(sh.ctx, inp.x[:, t0:t1].contiguous().to(gu.DEV), B, t1 - t0,
+                                 inp.R[t0:t1].contiguous().to(gu.DEV), True, ck, cv, T1 + T2, t0, d)
+                abi.attn_sync_status(sh.ctx)
+                total[:, t0:t1] += gu.np64(d)
+        finally:
+            sh.close()
+        shd = Shard(dec, g0, n)
+        try:
+            ck = dec.cache_k[:, :, g0:g0 + n].contiguous().to(gu.DEV)
+            cv = dec.cache_v[:, :, g0:g0 + n].contiguous().to(gu.DEV)
+            d = torch.empty(Bd, 1, 4096, dtype=torch.float32, device=gu.DEV)
+            abi.attn_decode(shd.ctx, dec.x.to(gu.DEV), Bd, pos, dec.R.to(gu.DEV), ck, cv, S_d, d)
+            abi.attn_sync_status(shd.ctx)
+            total_d += gu.np64(d)
+        finally:
+            shd.close()
+    gu.assert_close(total, ref, what="chunked prefill, sum of 2 shard partials")
+    gu.assert_close(total_d, ref_d, what="decode B=80, sum of 2 shard partials")

@@ -32,8 +32,9 @@ def nvcc() -> str:
 
 
 def _inputs_mtime() -> float:
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
+    src = (".cu", ".cuh", ".h")
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(src)]
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(src)]
     files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
 
