@@ -186,6 +186,35 @@ def test_decode_equals_last_prefill_row_on_gpu():
         blk.close()
 
 
+def test_prefill_then_three_decode_steps_against_oracle():
+    # prefill 300 positions of 3 sequences, then decode positions 300, 301, 302 one at a time
+    # through the same caches; every step's Delta against the oracle fed the oracle's own
+    # caches (rotated keys and values of all earlier positions)
+    B, T, steps = 3, 300, 3
+    inp = gin.make_custom(seed=77, B=B, T=T)
+    blk = gu.Block(inp)
+    try:
+        S_max = T + steps
+        ck, cv = gu.empty_cache(B, S_max)
+        blk.prefill(inp.x.to(gu.DEV), inp.R.to(gu.DEV), ck, cv)
+        wq, wk, wv, wo = blk.w64
+        _, ex = orc.attention_block(gin.to_f64(inp.x), wq, wk, wv, wo, gin.to_f64(inp.R), keep=True)
+        ok = np.zeros((B, S_max, 8, 128))
+        ov = np.zeros((B, S_max, 8, 128))
+        ok[:, :T], ov[:, :T] = ex["K_r"], ex["V"]
+        gen = torch.Generator().manual_seed(78)
+        for i in range(steps):
+            pos = T + i
+            x1 = torch.randn(B, 1, 4096, generator=gen).to(torch.bfloat16)
+            R1 = gin.rope_table([pos])
+            d = blk.decode(x1.to(gu.DEV), R1.to(gu.DEV), ck, cv, pos)
+            ref, ex1 = orc.attention_decode(gin.to_f64(x1), wq, wk, wv, wo, gin.to_f64(R1), ok, ov, pos, keep=True)
+            gu.assert_close(gu.np64(d), ref, what=f"decode step at position {pos}")
+            ok, ov = ex1["cache_k"], ex1["cache_v"]
+    finally:
+        blk.close()
+
+
 def test_prefill_maximum_token_count():
     # B*T at the documented limit (262144): GEMM M = 262144, 32768 attention CTAs, a 4 GB
     # workspace; a few sequences checked against the oracle
