@@ -323,9 +323,16 @@ def run_reference(args, w, inp):
     w64 = [gin.to_f64(t) for t in (inp.wq, inp.wk, inp.wv, inp.wo)]
     total_budget = 120.0
     if w.kind == "prefill":
-        dt, _ = oracle_sample_step(inp, w, 32, 1, w64)  # calibration
-        per_tok = dt / 32
-        n = int(max(16, min(w.T, total_budget / max(1, args.steps + args.warmup) / per_tok)))
+        # calibration at two prefix lengths; the oracle's time grows as a n + b n^2
+        # (projections, then the attention products), so size the prefix from that fit
+        n1, n2 = min(w.T, 512), min(w.T, 1024)
+        t1, _ = oracle_sample_step(inp, w, n1, 1, w64)
+        t2, _ = oracle_sample_step(inp, w, n2, 1, w64)
+        budget = total_budget / max(1, args.steps + args.warmup)
+        b = max((t2 / n2 - t1 / n1) / max(1, n2 - n1), 1e-12)
+        a = max(t1 / n1 - b * n1, 1e-9)
+        n_fit = (-a + (a * a + 4 * b * budget) ** 0.5) / (2 * b)
+        n = int(max(16, min(w.T, 4096, n_fit)))
         seqs = 1
         desc = f"oracle prefill of positions 0..{n - 1} of sequence 0 per step"
     else:
