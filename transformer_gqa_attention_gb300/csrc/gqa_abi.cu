@@ -12,6 +12,8 @@
 #include <mutex>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "gqa_attn.h"
 #include "launch.h"
 #include "pair_sched.h"
@@ -251,11 +253,24 @@ int take_fault(gqa_ctx* c, int kind) {
 constexpr size_t kMaxProfiledLaunches = 65536;
 
 // RAII bracket of one kernel launch with two events when profiling is on.
+// NVTX range names of the kernel kinds (host-side ranges around each launch; without a tool
+// attached an NVTX call returns at once).
+const char* const kKindNames[GQA_KERNEL_KINDS] = {"gqa.qkv_gemm", "gqa.qkv_splitk", "gqa.flash_prefill",
+                                                  "gqa.decode_attn", "gqa.out_gemm", "gqa.out_splitk",
+                                                  "gqa.rms_norm"};
+
+// RAII NVTX range around one entry point's host work (its launches nest inside it).
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+};
+
 struct ProfScope {
   gqa_ctx* c;
   cudaStream_t s;
   bool on;
   ProfScope(gqa_ctx* c_, int kind, cudaStream_t s_) : c(c_), s(s_), on(false) {
+    nvtxRangePushA(kind >= 0 && kind < GQA_KERNEL_KINDS ? kKindNames[kind] : "gqa.kernel");
     if (c->profiling && c->ev_used < kMaxProfiledLaunches) {
       if (c->ev.size() < 2 * (c->ev_used + 1)) {
         cudaEvent_t a, b;
@@ -274,6 +289,7 @@ struct ProfScope {
       cudaEventRecord(c->ev[2 * c->ev_used + 1], s);
       ++c->ev_used;
     }
+    nvtxRangePop();
   }
 };
 
@@ -611,6 +627,7 @@ extern "C" {
 
 gqa_status attn_prefill(gqa_ctx* c, const void* x, int B, int T, const float* R, int causal, void* cache_k,
                         void* cache_v, int S_max, int start_pos, float* delta, gqa_stream_t stream) {
+  CallRange range("gqa.attn_prefill");
   return prefill_impl(c, x, B, T, R, causal, cache_k, cache_v, S_max, start_pos, delta, false,
                       reinterpret_cast<cudaStream_t>(stream));
 }
@@ -618,18 +635,21 @@ gqa_status attn_prefill(gqa_ctx* c, const void* x, int B, int T, const float* R,
 gqa_status attn_prefill_residual(gqa_ctx* c, const void* x, int B, int T, const float* R, int causal,
                                  void* cache_k, void* cache_v, int S_max, int start_pos, float* h_out,
                                  gqa_stream_t stream) {
+  CallRange range("gqa.attn_prefill_residual");
   return prefill_impl(c, x, B, T, R, causal, cache_k, cache_v, S_max, start_pos, h_out, true,
                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 gqa_status attn_decode(gqa_ctx* c, const void* x, int B, int start_pos, const float* R_row, void* cache_k,
                        void* cache_v, int S_max, float* delta, gqa_stream_t stream) {
+  CallRange range("gqa.attn_decode");
   return decode_impl(c, x, B, start_pos, R_row, cache_k, cache_v, S_max, delta, false,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 gqa_status attn_decode_residual(gqa_ctx* c, const void* x, int B, int start_pos, const float* R_row,
                                 void* cache_k, void* cache_v, int S_max, float* h_out, gqa_stream_t stream) {
+  CallRange range("gqa.attn_decode_residual");
   return decode_impl(c, x, B, start_pos, R_row, cache_k, cache_v, S_max, h_out, true,
                      reinterpret_cast<cudaStream_t>(stream));
 }
