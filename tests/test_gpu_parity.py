@@ -152,6 +152,47 @@ def test_decode_small():
         blk.close()
 
 
+@pytest.mark.parametrize("pos", [0, 63, 64, 65, 1000])
+def test_decode_at_tile_boundaries_and_first_position(pos):
+    # kv_len = pos + 1 around the 64-key tile of the split-KV kernel; pos = 0 attends over the
+    # new token alone, so H of head h is exactly the new V of its kv head h // 4 (rounded once)
+    B = 2
+    inp = gin.make_custom(seed=200 + pos, B=B, T=1, start_pos=pos, S_max=pos + 1, fill_cache=True)
+    blk = gu.Block(inp)
+    try:
+        ck, cv = inp.cache_k.to(gu.DEV), inp.cache_v.to(gu.DEV)
+        delta = blk.decode(inp.x.to(gu.DEV), inp.R.to(gu.DEV), ck, cv, pos)
+        wq, wk, wv, wo = blk.w64
+        ref, ex = orc.attention_decode(gin.to_f64(inp.x), wq, wk, wv, wo, gin.to_f64(inp.R),
+                                       gin.to_f64(inp.cache_k), gin.to_f64(inp.cache_v), pos, keep=True)
+        gu.assert_close(gu.np64(delta), ref, what=f"decode at position {pos}")
+        if pos == 0:
+            _, h = blk.intermediates(B)
+            v_new = gu.np64(cv[:, 0])  # [B, 8, 128] as stored by the kernel (bf16)
+            expect = np.repeat(v_new, 4, axis=1).reshape(B, 4096)
+            np.testing.assert_array_equal(gu.np64(h), expect)
+    finally:
+        blk.close()
+
+
+@pytest.mark.parametrize("T,start_pos", [(1, 5), (1, 300), (3, 129), (17, 1000)])
+def test_short_prefill_continuing_a_long_cache(T, start_pos):
+    B = 2
+    full = gin.make_custom(seed=210 + T, B=B, T=start_pos + T)
+    blk = gu.Block(full)
+    try:
+        S_max = start_pos + T
+        ck, cv = gu.empty_cache(B, S_max)
+        x, R = full.x.to(gu.DEV), full.R.to(gu.DEV)
+        blk.prefill(x[:, :start_pos].contiguous(), R[:start_pos].contiguous(), ck, cv)
+        d = blk.prefill(x[:, start_pos:].contiguous(), R[start_pos:].contiguous(), ck, cv, start_pos=start_pos)
+        rows = np.arange(start_pos, start_pos + T)
+        ref, _ = gu.oracle_prefill(blk, full, rows=rows)
+        gu.assert_close(gu.np64(d), ref, what=f"prefill of {T} positions after {start_pos}")
+    finally:
+        blk.close()
+
+
 def test_decode_b64_pos4095_workload_sampled_sequences():
     inp = gin.make_inputs("decode_b64_pos4095")
     pos = 4095
