@@ -318,6 +318,16 @@ def _one_core_child(name: str, budget_s: float):
     print(json.dumps(rec))
 
 
+def prefix_for_budget(n1, t1, n2, t2, budget_s, T, cap=4096):
+    """Causal-prefix length whose oracle time fits budget_s, from the times t1, t2 measured at
+    prefix lengths n1 < n2 under t(n) = a n + b n^2 (the projections grow with n, the
+    attention products with n^2); between 16 and min(T, cap)."""
+    b = max((t2 / n2 - t1 / n1) / max(1, n2 - n1), 1e-12)
+    a = max(t1 / n1 - b * n1, 1e-9)
+    n_fit = (-a + (a * a + 4 * b * budget_s) ** 0.5) / (2 * b)
+    return int(max(16, min(T, cap, n_fit)))
+
+
 def run_reference(args, w, inp):
     """The oracle as the reference arm: W untimed + K timed steps, each a bounded sample."""
     w64 = [gin.to_f64(t) for t in (inp.wq, inp.wk, inp.wv, inp.wo)]
@@ -328,11 +338,7 @@ def run_reference(args, w, inp):
         n1, n2 = min(w.T, 512), min(w.T, 1024)
         t1, _ = oracle_sample_step(inp, w, n1, 1, w64)
         t2, _ = oracle_sample_step(inp, w, n2, 1, w64)
-        budget = total_budget / max(1, args.steps + args.warmup)
-        b = max((t2 / n2 - t1 / n1) / max(1, n2 - n1), 1e-12)
-        a = max(t1 / n1 - b * n1, 1e-9)
-        n_fit = (-a + (a * a + 4 * b * budget) ** 0.5) / (2 * b)
-        n = int(max(16, min(w.T, 4096, n_fit)))
+        n = prefix_for_budget(n1, t1, n2, t2, total_budget / max(1, args.steps + args.warmup), w.T)
         seqs = 1
         desc = f"oracle prefill of positions 0..{n - 1} of sequence 0 per step"
     else:

@@ -1,0 +1,57 @@
+"""Host logic of bench.py (CPU): the algorithmic work it divides by, checked against the
+figures worked out from the block's shapes (41,943,040 parameters, causal pairs T(T+1)/2 per
+head, bf16 K/V cache of 8 heads x 128), and the sizing of the oracle's timed prefix."""
+import pytest
+
+import bench
+from transformer_gqa_attention_gb300 import inputs as gin
+
+
+def test_prefill_flops_of_the_workloads():
+    # projections 2 x 41,943,040 per token; causal attention 4 x 128 x 32 x T(T+1)/2 per sequence
+    # = 8192 T(T+1); the rounded totals are the ones worked out for the workloads (GFLOP)
+    for (B, T, proj_g, attn_g) in [(1, 16, 1.342, 0.002228), (1, 2048, 171.80, 34.38),
+                                   (4, 8192, 2748.78, 2199.29), (1, 32768, 2748.78, 8796.36)]:
+        proj, attn = bench.prefill_flops(B, T)
+        assert proj == 2 * 41_943_040 * B * T
+        assert attn == 8192 * T * (T + 1) * B
+        assert abs(proj / 1e9 - proj_g) < 0.01 * proj_g and abs(attn / 1e9 - attn_g) < 0.001 * attn_g
+    # a causal prefix continuing a cache sees its start_pos earlier keys in full
+    _, a = bench.prefill_flops(1, 1, start_pos=9)
+    assert a == 4 * 128 * 32 * 10
+    _, a_nc = bench.prefill_flops(1, 4, causal=False)
+    assert a_nc == 4 * 128 * 32 * 16
+
+
+def test_decode_bytes_of_the_workload():
+    # KV 64 x 4096 x 8 x 128 x 2 B x 2 + weights 2 x 41,943,040 B + x in + Delta out + new K/V
+    assert bench.decode_bytes(64, 4096) == 1_159_462_912
+
+
+def test_kernel_work_models():
+    w = gin.WORKLOADS["prefill_b1_t2048"]
+    assert bench.kernel_work("qkv_gemm", w) == ("tensor", 2.0 * 2048 * 4096 * 6144, "TFLOP/s")
+    assert bench.kernel_work("out_gemm", w)[1] == 2.0 * 2048 * 4096 * 4096
+    assert bench.kernel_work("flash_prefill", w)[1] == 8192 * 2048 * 2049
+    d = gin.WORKLOADS["decode_b64_pos4095"]
+    assert bench.kernel_work("decode_attn", d) == ("hbm", float(64 * 4096 * 8 * 128 * 4 + 64 * 4096 * 2), "GB/s")
+    assert bench.kernel_work("nonexistent", d) == (None, None, None)
+
+
+def test_prefix_sizing_follows_the_quadratic_model():
+    # times generated from t(n) = a n + b n^2: the chosen prefix meets the budget
+    a, b = 1e-3, 2e-6
+    t = lambda n: a * n + b * n * n
+    n = bench.prefix_for_budget(512, t(512), 1024, t(1024), 5.0, 32768)
+    assert t(n) <= 5.0 < t(n + 2)
+    # a linear model would have picked ~5000 positions here; the cap and T bound it
+    assert bench.prefix_for_budget(512, t(512), 1024, t(1024), 1e6, 32768) == 4096
+    assert bench.prefix_for_budget(512, t(512), 1024, t(1024), 1e6, 700) == 700
+    assert bench.prefix_for_budget(512, t(512), 1024, t(1024), 1e-9, 32768) == 16
+
+
+@pytest.mark.parametrize("name", sorted(gin.WORKLOADS))
+def test_workload_config_names_the_workload(name):
+    w = gin.WORKLOADS[name]
+    c = bench.workload_config(w)
+    assert c["workload"] == name and c["B"] == w.B and c["T"] == w.T and c["S_max"] == w.s_max
