@@ -45,42 +45,44 @@ NORM_EPS = 1e-5  # attention_norm epsilon of the residual workloads (norm_eps of
 
 
 # ------------------------------------------------------------------ accounting
-def prefill_flops(B, T, start_pos=0, causal=True):
+def prefill_flops(B, T, start_pos=0, causal=True, n_kv=8):
     """Algorithmic FLOPs: 2 x 41,943,040 per token for the projections plus 4*128 per
-    visible (query, key) pair per query head (QK^T and PV)."""
-    proj = 2 * 41_943_040 * B * T
+    visible (query, key) pair per query head (QK^T and PV).  A shard of n_kv of the 8 kv
+    groups holds n_kv/8 of the weights and of the query heads."""
+    proj = 2 * (41_943_040 // 8) * n_kv * B * T
     if causal:
         pairs = T * start_pos + T * (T + 1) // 2
     else:
         pairs = T * (start_pos + T)
-    return proj, 4 * 128 * 32 * pairs * B
+    return proj, 4 * 128 * 4 * n_kv * pairs * B
 
 
-def decode_bytes(B, kv_len):
-    """Minimum HBM bytes of one decode step: the K/V cache read (kv_len keys x 8 heads x
-    128 x bf16, K and V), the weights (W_QKV + W_O), x in, Delta out (fp32), the new K/V
-    entries written."""
-    kv = B * kv_len * 8 * 128 * 2 * 2
-    w = 41_943_040 * 2
-    return kv + w + B * 4096 * 2 + B * 4096 * 4 + B * 1024 * 2 * 2
+def decode_bytes(B, kv_len, n_kv=8):
+    """Minimum HBM bytes of one decode step: the K/V cache read (kv_len keys x n_kv heads x
+    128 x bf16, K and V), the weights (W_QKV + W_O, n_kv/8 of them for a shard), x in, Delta
+    out (fp32), the new K/V entries written."""
+    kv = B * kv_len * n_kv * 128 * 2 * 2
+    w = (41_943_040 // 8) * n_kv * 2
+    return kv + w + B * 4096 * 2 + B * 4096 * 4 + B * n_kv * 128 * 2 * 2
 
 
 def kernel_work(kind, w: gin.Workload):
     """(bound, algorithmic work per launch, unit) of one kernel kind on the workload."""
     n_tok = w.n_tok
+    g = w.n_kv  # kv groups of the context: Q/K/V rows 768 g, W_O columns 512 g
     if kind == "qkv_gemm":
-        return "tensor", 2.0 * n_tok * 4096 * 6144, "TFLOP/s"
+        return "tensor", 2.0 * n_tok * 4096 * 768 * g, "TFLOP/s"
     if kind == "out_gemm":
-        return "tensor", 2.0 * n_tok * 4096 * 4096, "TFLOP/s"
+        return "tensor", 2.0 * n_tok * 512 * g * 4096, "TFLOP/s"
     if kind == "flash_prefill":
-        return "tensor", float(prefill_flops(w.B, w.T, w.start_pos, w.causal)[1]), "TFLOP/s"
+        return "tensor", float(prefill_flops(w.B, w.T, w.start_pos, w.causal, g)[1]), "TFLOP/s"
     if kind == "decode_attn":
         kv_len = w.start_pos + 1
-        return "hbm", float(w.B * kv_len * 8 * 128 * 2 * 2 + w.B * 4096 * 2), "GB/s"
+        return "hbm", float(w.B * kv_len * g * 128 * 2 * 2 + w.B * 512 * g * 2), "GB/s"
     if kind == "qkv_splitk":
-        return "hbm", float(6144 * 4096 * 2 + n_tok * 4096 * 2), "GB/s"
+        return "hbm", float(768 * g * 4096 * 2 + n_tok * 4096 * 2), "GB/s"
     if kind == "out_splitk":
-        return "hbm", float(4096 * 4096 * 2 + n_tok * 4096 * 2), "GB/s"
+        return "hbm", float(4096 * 512 * g * 2 + n_tok * 512 * g * 2), "GB/s"
     if kind == "rms_norm":
         return "hbm", float(n_tok * 4096 * 2 + n_tok * 4), "GB/s"
     return None, None, None
@@ -375,6 +377,10 @@ def workload_config(w: gin.Workload):
     if w.residual:
         c.update(residual=True, norm_eps=NORM_EPS,
                  form="h = x + Delta_attn(attention_norm(x)); attention_norm weight 1 + 0.1 N(0,1)")
+    if w.n_kv != 8:
+        c.update(n_kv_heads=w.n_kv, n_heads=4 * w.n_kv,
+                 form=f"one rank of a {8 // w.n_kv}-way head-sharded split: kv groups 0..{w.n_kv - 1}, "
+                      "partial Delta (the all-reduce over ranks is not part of the step)")
     return c
 
 
@@ -387,12 +393,17 @@ def measure_gpu(args, w: gin.Workload, inp, world, rank, local, steps, warmup):
     dev = torch.device("cuda", local)
     B, T = w.B, w.T
     S_max = w.s_max
-    wts = [t.to(dev) for t in (inp.wq, inp.wk, inp.wv, inp.wo)]
+    G = w.n_kv
+    if G == 8:
+        wts = [t.to(dev) for t in (inp.wq, inp.wk, inp.wv, inp.wo)]
+    else:  # one tensor-parallel rank: kv groups 0 .. G-1 and their query heads
+        from transformer_gqa_attention_gb300 import tp
+        wts = [t.to(dev) for t in tp.shard_weights(inp.wq, inp.wk, inp.wv, inp.wo, 0, G)]
     stream = torch.cuda.current_stream(dev)
     norm_w = gin.norm_weight(w.seed).to(dev) if w.residual else None
 
     def new_ctx():
-        c = abi.attn_create(*wts)
+        c = abi.attn_create(*wts) if G == 8 else abi.attn_create_shard(*wts, G)
         if w.residual:
             abi.attn_set_norm(c, norm_w, NORM_EPS, stream)
         return c
@@ -401,7 +412,7 @@ def measure_gpu(args, w: gin.Workload, inp, world, rank, local, steps, warmup):
     x = inp.x.to(dev)
     R = inp.R.to(dev)
     if w.kind == "prefill":
-        ck = torch.zeros(B, S_max, 8, 128, dtype=torch.bfloat16, device=dev)
+        ck = torch.zeros(B, S_max, G, 128, dtype=torch.bfloat16, device=dev)
         cv = torch.zeros_like(ck)
         delta = torch.empty(B, T, 4096, dtype=torch.float32, device=dev)
         fn = abi.attn_prefill_residual if w.residual else abi.attn_prefill
@@ -409,8 +420,8 @@ def measure_gpu(args, w: gin.Workload, inp, world, rank, local, steps, warmup):
         def step(xd=x, Rd=R, out=delta, c=ctx):
             fn(c, xd, B, T, Rd, w.causal, ck, cv, S_max, w.start_pos, out, stream)
     else:
-        ck = inp.cache_k.to(dev)
-        cv = inp.cache_v.to(dev)
+        ck = inp.cache_k[:, :, :G].contiguous().to(dev)
+        cv = inp.cache_v[:, :, :G].contiguous().to(dev)
         delta = torch.empty(B, 1, 4096, dtype=torch.float32, device=dev)
         fn = abi.attn_decode_residual if w.residual else abi.attn_decode
 
@@ -524,14 +535,14 @@ def measure_gpu(args, w: gin.Workload, inp, world, rank, local, steps, warmup):
     peaks, peak_src = load_peaks()
     n = world
     if w.kind == "prefill":
-        proj, attn = prefill_flops(B, T, w.start_pos, w.causal)
+        proj, attn = prefill_flops(B, T, w.start_pos, w.causal, G)
         value = n * B * T / (ms / 1e3)
         unit = "tokens/s"
         e2e_value = n * B * T / (e2e_ms / 1e3)
         extra = {"tflops": n * (proj + attn) / (ms / 1e3) / 1e12,
                  "tflops_frac_of_" + peak_src: (proj + attn) / (ms / 1e3) / 1e12 / peaks["bf16_tflops"]}
     else:
-        by = decode_bytes(B, w.start_pos + 1)
+        by = decode_bytes(B, w.start_pos + 1, G)
         value = n * by / (ms / 1e3) / 1e9
         unit = "GB/s"
         e2e_value = n * by / (e2e_ms / 1e3) / 1e9
@@ -596,7 +607,7 @@ def run_gpu(args, w: gin.Workload, world, rank, local):
         return
     if subs:
         line["sub_records"] = subs
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and w.n_kv == 8:
         line["cpu_baseline"] = cpu_baseline(inp, w)
         line["cpu_baseline"]["single_core"] = {name: single_core_baseline(name) for name in SINGLE_CORE_WORKLOADS}
     print(json.dumps(line))
@@ -622,6 +633,8 @@ def main():
     world, rank, local = dist_setup(args.gpus)
     w = gin.WORKLOADS[args.workload]
     if args.impl == "reference":
+        if w.n_kv != 8:
+            raise SystemExit("the reference arm times the whole block: choose a whole-block workload")
         if rank == 0:
             run_reference(args, w, gin.make_inputs(w))
         return

@@ -55,3 +55,18 @@ def test_workload_config_names_the_workload(name):
     w = gin.WORKLOADS[name]
     c = bench.workload_config(w)
     assert c["workload"] == name and c["B"] == w.B and c["T"] == w.T and c["S_max"] == w.s_max
+
+
+def test_shard_accounting_is_the_whole_divided_by_the_split():
+    for n in (1, 2, 4):
+        p8, a8 = bench.prefill_flops(1, 2048)
+        pn, an = bench.prefill_flops(1, 2048, n_kv=n)
+        assert pn * 8 == p8 * n and an * 8 == a8 * n
+    # a decode shard reads its share of the cache and of the weights; x and Delta stay whole
+    whole = bench.decode_bytes(64, 4096)
+    part = bench.decode_bytes(64, 4096, n_kv=1)
+    assert part == 64 * 4096 * 128 * 4 + 41_943_040 * 2 // 8 + 64 * 4096 * 6 + 64 * 128 * 4
+    assert part < whole / 7
+    w = gin.WORKLOADS["prefill_b1_t2048_tp8"]
+    assert bench.kernel_work("qkv_gemm", w)[1] == 2.0 * 2048 * 4096 * 768
+    assert bench.kernel_work("out_gemm", w)[1] == 2.0 * 2048 * 512 * 4096

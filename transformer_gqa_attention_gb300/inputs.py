@@ -45,6 +45,7 @@ class Workload:
     start_pos: int = 0
     S_max: int = 0  # 0 -> start_pos + T
     residual: bool = False  # attention_norm in front and the residual add behind
+    n_kv: int = 8  # kv groups run: 8 = the whole block; fewer = one tensor-parallel shard
 
     @property
     def s_max(self) -> int:
@@ -70,6 +71,12 @@ WORKLOADS = {
         Workload("prefill_b1_t2048_residual", "prefill", B=1, T=2048, seed=1, residual=True),
         Workload("decode_b64_pos4095_residual", "decode", B=64, T=1, seed=3, start_pos=4095, S_max=4096,
                  residual=True),
+        # one rank's share of a head-sharded 8-way (1 kv group) or 2-way (4 kv groups) split:
+        # the same inputs, the shard's weight slices and its own cache
+        Workload("prefill_b1_t32768_tp8", "prefill", B=1, T=32768, seed=4, n_kv=1),
+        Workload("prefill_b1_t32768_tp2", "prefill", B=1, T=32768, seed=4, n_kv=4),
+        Workload("prefill_b1_t2048_tp8", "prefill", B=1, T=2048, seed=1, n_kv=1),
+        Workload("decode_b64_pos4095_tp8", "decode", B=64, T=1, seed=3, start_pos=4095, S_max=4096, n_kv=1),
     ]
 }
 
