@@ -77,8 +77,10 @@ def kernel_work(kind, w: gin.Workload):
     if kind == "flash_prefill":
         return "tensor", float(prefill_flops(w.B, w.T, w.start_pos, w.causal, g)[1]), "TFLOP/s"
     if kind == "decode_attn":
-        kv_len = w.start_pos + 1
-        return "hbm", float(w.B * kv_len * g * 128 * 2 * 2 + w.B * 512 * g * 2), "GB/s"
+        # decode, or a prefill of T <= 16 positions (same kernel): K and V of the whole cache
+        # once, q in and H out
+        kv_len = w.start_pos + w.T
+        return "hbm", float(w.B * kv_len * g * 128 * 2 * 2 + 2 * n_tok * 512 * g * 2), "GB/s"
     if kind == "qkv_splitk":
         return "hbm", float(768 * g * 4096 * 2 + n_tok * 4096 * 2), "GB/s"
     if kind == "out_splitk":

@@ -34,7 +34,11 @@ def test_kernel_work_models():
     assert bench.kernel_work("out_gemm", w)[1] == 2.0 * 2048 * 4096 * 4096
     assert bench.kernel_work("flash_prefill", w)[1] == 8192 * 2048 * 2049
     d = gin.WORKLOADS["decode_b64_pos4095"]
-    assert bench.kernel_work("decode_attn", d) == ("hbm", float(64 * 4096 * 8 * 128 * 4 + 64 * 4096 * 2), "GB/s")
+    # K and V of 4096 positions, q read and H written (64 x 4096 bf16 each)
+    assert bench.kernel_work("decode_attn", d) == ("hbm", float(64 * 4096 * 8 * 128 * 4 + 2 * 64 * 4096 * 2), "GB/s")
+    # a 16-token prefill runs the same kernel: the 16 cached positions, 16 query rows in and out
+    s = gin.WORKLOADS["prefill_b1_t16"]
+    assert bench.kernel_work("decode_attn", s)[1] == float(16 * 8 * 128 * 4 + 2 * 16 * 4096 * 2)
     assert bench.kernel_work("nonexistent", d) == (None, None, None)
 
 

@@ -8,7 +8,7 @@ namespace gqa {
 cudaError_t configure_gemm_kernels();
 
 size_t flash_smem() { return FlashSmem::kBytes; }
-size_t decode_smem() { return DecodeSmem::kBytes; }
+size_t decode_smem() { return DecodeSmemT<4>::kBytes; }
 
 cudaError_t configure_kernels() {
   cudaError_t e = configure_gemm_kernels();
@@ -16,8 +16,11 @@ cudaError_t configure_kernels() {
   e = cudaFuncSetAttribute(flash_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            FlashSmem::kBytes);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(decode_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              DecodeSmem::kBytes);
+  e = cudaFuncSetAttribute(decode_attn_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           DecodeSmemT<4>::kBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(decode_attn_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              DecodeSmemT<16>::kBytes);
 }
 
 cudaError_t launch_flash_prefill(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
@@ -27,7 +30,12 @@ cudaError_t launch_flash_prefill(const CUtensorMap& q, const CUtensorMap& k, con
 
 cudaError_t launch_decode_attn(const CUtensorMap& k, const CUtensorMap& v, const DecodeParams& p,
                                dim3 grid, cudaStream_t s) {
-  return launch_pdl(decode_attn_kernel, grid, dim3(160), DecodeSmem::kBytes, s, 0, k, v, p);
+  return launch_pdl(decode_attn_kernel<1>, grid, dim3(160), DecodeSmemT<4>::kBytes, s, 0, k, v, p);
+}
+
+cudaError_t launch_short_attn(const CUtensorMap& k, const CUtensorMap& v, const DecodeParams& p, dim3 grid,
+                              cudaStream_t s) {
+  return launch_pdl(decode_attn_kernel<4>, grid, dim3(160), DecodeSmemT<16>::kBytes, s, 0, k, v, p);
 }
 
 // Both exponentials of the softmax on n inputs (the FMA-pipe cubic and the multi-function

@@ -165,6 +165,10 @@ extern "C" gqa_status attn_decode_attention_noalloc(const void* q_r, const void*
   p.kv_len = kv_len;
   p.n_splits = splits;
   p.tiles_per_split = tiles_per_split;
+  p.T = 1;
+  p.q_start = kv_len - 1;
+  p.causal = 0;  // one position per sequence, seeing the whole cache
+  p.n_pg = 1;
   p.q = q_r;
   p.part_o = su->scratch;
   p.part_ml = su->scratch + kPartOFloats;

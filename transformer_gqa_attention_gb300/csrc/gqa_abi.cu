@@ -76,8 +76,13 @@ constexpr long long kMaxTokens = 262144;
 constexpr long long kMaxSMax = 1048576;
 constexpr int kSkinnyMaxTokens = 64;     // at or below: swap-AB split-K projections
 constexpr int kDecodeMaxBatch = 1024;
-// Arrival counters of the decode split merge, one per (sequence, kv group).
+// Arrival counters of the decode split merge, one per (sequence, kv group, position group).
 constexpr int kCounterInts = kDecodeMaxBatch * 8;
+// Prefills of at most this many tokens per sequence run the decode attention kernel with
+// kShortPos positions per CTA instead of the flash kernel (whose 128-row query tiles they
+// would fill to an eighth at most).
+constexpr int kShortMaxT = 16;
+constexpr int kShortPos = 4;
 
 // ------------------------------------------------------------------ tensor maps
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -184,12 +189,15 @@ struct DecodePlan {
   int n_splits, tiles_per_split;
 };
 
-DecodePlan decode_plan(int B, int n_kv, int kv_len, int num_sms) {
+// Key splits of the decode attention kernel for `units` (sequence, position group) pairs of
+// n_kv groups each, at ctas_per_sm resident CTAs per SM (2 with one position per CTA, 1 with
+// four: the larger reduction scratch).
+DecodePlan decode_plan(int units_b, int n_kv, int kv_len, int num_sms, int ctas_per_sm = 2) {
   const int n_tiles = (kv_len + kDecTileKeys - 1) / kDecTileKeys;
-  // aim for ~6-7 waves of two CTAs per SM, at least 4 tiles (256 keys) per split (B=64 at
-  // 4096 keys: 4 splits of 16 tiles measured faster than 5, 8 or 10)
-  const long long units = static_cast<long long>(B) * n_kv;
-  const long long target = 13LL * num_sms;
+  // aim for ~6-7 waves, at least 4 tiles (256 keys) per split (B=64 at 4096 keys: 4 splits of
+  // 16 tiles measured faster than 5, 8 or 10)
+  const long long units = static_cast<long long>(units_b) * n_kv;
+  const long long target = 13LL * num_sms * ctas_per_sm / 2;
   int splits = static_cast<int>(std::max(1LL, (target + units - 1) / units));
   splits = std::min(splits, std::max(1, n_tiles / 4));
   DecodePlan d;
@@ -198,7 +206,8 @@ DecodePlan decode_plan(int B, int n_kv, int kv_len, int num_sms) {
   return d;
 }
 
-WsLayout ws_layout(long long n_tok, int n_kv, const SkinnyPlan* sk, const DecodePlan* dp, int B_dec) {
+// dec_rows: rows of decode partials per (kv group, split): B x position groups x rows per CTA.
+WsLayout ws_layout(long long n_tok, int n_kv, const SkinnyPlan* sk, const DecodePlan* dp, long long dec_rows) {
   WsLayout w{};
   size_t off = 0;
   const size_t q_cols = static_cast<size_t>(n_kv) * 512;
@@ -209,10 +218,10 @@ WsLayout ws_layout(long long n_tok, int n_kv, const SkinnyPlan* sk, const Decode
   w.dec_o_off = off;
   w.dec_ml_off = off;
   if (dp) {
-    const size_t units = static_cast<size_t>(B_dec) * n_kv * dp->n_splits;
-    off = round_up(off + units * 4 * 128 * 4, 256);
+    const size_t rows = static_cast<size_t>(dec_rows) * n_kv * dp->n_splits;
+    off = round_up(off + rows * 128 * 4, 256);
     w.dec_ml_off = off;
-    off = round_up(off + units * 4 * 2 * 4, 256);
+    off = round_up(off + rows * 2 * 4, 256);
   }
   w.rstd_off = off;  // residual form: 1 / rms per token row
   off = round_up(off + static_cast<size_t>(n_tok) * 4, 256);
@@ -502,9 +511,15 @@ gqa_status prefill_impl(gqa_ctx* c, const void* x, int B, int T, const float* R,
 
   const int n_tok = B * T;
   const int G = c->n_kv;
+  const int kv_len = start_pos + T;
   SkinnyPlan sk_v = skinny_plan(n_tok, c->num_sms);
   const SkinnyPlan* sk = n_tok <= kSkinnyMaxTokens ? &sk_v : nullptr;
-  const WsLayout w = ws_layout(n_tok, G, sk, nullptr, 0);
+  // few positions per sequence: the decode attention kernel, 4 positions per CTA
+  const int n_pg = (T + kShortPos - 1) / kShortPos;
+  const bool short_path = T <= kShortMaxT && static_cast<long long>(B) * G * n_pg <= kCounterInts;
+  const DecodePlan dp = decode_plan(B * n_pg, G, kv_len, c->num_sms, 1);
+  const WsLayout w = short_path ? ws_layout(n_tok, G, sk, &dp, static_cast<long long>(B) * n_pg * 4 * kShortPos)
+                                : ws_layout(n_tok, G, sk, nullptr, 0);
   st = ensure_ws(c, w.total, s);
   if (st != GQA_OK) return st;
   void* q_r = c->ws + w.q_off;
@@ -520,8 +535,38 @@ gqa_status prefill_impl(gqa_ctx* c, const void* x, int B, int T, const float* R,
   st = run_qkv(c, x, n_tok, T, R, cache_k, cache_v, S_max, start_pos, q_r, w, sk, row_scale, s);
   if (st != GQA_OK) return st;
 
+  if (short_path) {
+    // steps 6-13 for T <= 16 positions: query t sees keys 0 .. start_pos + t (causal) or all
+    CUtensorMap tk, tv;
+    if (!map_cache(&tk, cache_k, B, S_max, G, kv_len, kDecTileKeys) ||
+        !map_cache(&tv, cache_v, B, S_max, G, kv_len, kDecTileKeys))
+      return cuda_fail(cudaErrorInvalidValue);
+    DecodeParams p{};
+    p.B = B;
+    p.n_kv = G;
+    p.kv_len = kv_len;
+    p.n_splits = dp.n_splits;
+    p.tiles_per_split = dp.tiles_per_split;
+    p.T = T;
+    p.q_start = start_pos;
+    p.causal = causal ? 1 : 0;
+    p.n_pg = n_pg;
+    p.q = q_r;
+    p.part_o = reinterpret_cast<float*>(c->ws + w.dec_o_off);
+    p.part_ml = reinterpret_cast<float*>(c->ws + w.dec_ml_off);
+    p.H = h;
+    p.status = c->status;
+    p.scale_log2 = kScaleLog2;
+    p.counters = c->counters;
+    p.fault = take_fault(c, GQA_KERNEL_DECODE_ATTN);
+    {
+      ProfScope ps(c, GQA_KERNEL_DECODE_ATTN, s);
+      GQA_CUDA(launch_short_attn(tk, tv, p, dim3(dp.n_splits, G, B * n_pg), s));
+    }
+    return run_out(c, h, n_tok, delta, w, sk, residual ? x : nullptr, s);
+  }
+
   // steps 6-13: causal GQA flash attention over keys 0 .. start_pos+T-1
-  const int kv_len = start_pos + T;
   CUtensorMap tq, tk, tv, th;
   {
     // Q_r (read) and H (written) are both [B, T, 512 G] bf16, addressed in 64 x 128 boxes
@@ -579,7 +624,7 @@ gqa_status decode_impl(gqa_ctx* c, const void* x, int B, int start_pos, const fl
   SkinnyPlan sk_v = skinny_plan(B, c->num_sms);
   const SkinnyPlan* sk = B <= kSkinnyMaxTokens ? &sk_v : nullptr;
   const DecodePlan dp = decode_plan(B, G, kv_len, c->num_sms);
-  const WsLayout w = ws_layout(B, G, sk, &dp, B);
+  const WsLayout w = ws_layout(B, G, sk, &dp, static_cast<long long>(B) * 4);
   st = ensure_ws(c, w.total, s);
   if (st != GQA_OK) return st;
   void* q_r = c->ws + w.q_off;
@@ -607,6 +652,10 @@ gqa_status decode_impl(gqa_ctx* c, const void* x, int B, int start_pos, const fl
   p.kv_len = kv_len;
   p.n_splits = dp.n_splits;
   p.tiles_per_split = dp.tiles_per_split;
+  p.T = 1;
+  p.q_start = start_pos;
+  p.causal = 0;  // the new position sees the whole cache
+  p.n_pg = 1;
   p.q = q_r;
   p.part_o = reinterpret_cast<float*>(c->ws + w.dec_o_off);
   p.part_ml = reinterpret_cast<float*>(c->ws + w.dec_ml_off);

@@ -71,6 +71,9 @@ cudaError_t launch_flash_prefill(const CUtensorMap& q, const CUtensorMap& k, con
                                  const CUtensorMap& h, const FlashParams& p, dim3 grid, cudaStream_t s);
 cudaError_t launch_decode_attn(const CUtensorMap& k, const CUtensorMap& v, const DecodeParams& p,
                                dim3 grid, cudaStream_t s);
+// Short prefills (T <= 16): the decode attention kernel with 4 positions per CTA.
+cudaError_t launch_short_attn(const CUtensorMap& k, const CUtensorMap& v, const DecodeParams& p, dim3 grid,
+                              cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeParams& p, int B, cudaStream_t s);
 cudaError_t launch_exp2_compare(const float* a, float* out_fma, float* out_mufu, int n, cudaStream_t s);
 cudaError_t launch_rms_rstd(const void* x, int rows, float eps, float* r, cudaStream_t s);

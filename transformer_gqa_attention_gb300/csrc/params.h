@@ -63,11 +63,15 @@ constexpr int kDecTileKeys = 64;
 struct DecodeParams {
   int B, kv_len, n_splits, tiles_per_split;
   int n_kv;       // kv groups of the context (4 query heads each; q and H rows are 512 n_kv wide)
-  const void* q;  // [B, 512 n_kv] bf16 rotated queries
-  float* part_o;           // [B, n_kv, n_splits, 4, 128]
-  float* part_ml;          // [B, n_kv, n_splits, 4, 2]
-  int* counters;           // [B*n_kv] arrival counters: the last split merges (null: separate merge kernel)
-  void* H;        // [B, 512 n_kv] bf16 (combine output)
+  // query positions: T per sequence, the first at absolute position q_start (decode: T = 1,
+  // q_start = kv_len - 1); with causal, query t sees keys 0 .. q_start + t, else all kv_len
+  int T, q_start, causal;
+  int n_pg;       // position groups per sequence (ceil(T / positions per CTA))
+  const void* q;  // [B, T, 512 n_kv] bf16 rotated queries
+  float* part_o;           // [B, n_kv, n_pg, n_splits, rows, 128]
+  float* part_ml;          // [B, n_kv, n_pg, n_splits, rows, 2]
+  int* counters;           // [B*n_kv*n_pg] arrival counters: the last split merges (null: separate merge kernel)
+  void* H;        // [B, T, 512 n_kv] bf16 (combine output)
   int* status;
   // decode_combine_kernel only: when *status is non-zero (a split of this call gave up a
   // wait), H is written as NaN and the status bits are OR-ed into *status_sticky (null: not)
