@@ -74,9 +74,17 @@ __device__ __forceinline__ QkvRows qkv_rows(const GemmParams& p, int lane, int m
     const int mc = min(q.m[k], p.M - 1);
     q.b[k] = mc / p.T;
     q.t[k] = mc - q.b[k] * p.T;
-    q.rs[k] = p.row_scale ? __ldg(p.row_scale + mc) : 1.f;
+    q.rs[k] = 1.f;
   }
   return q;
+}
+
+// The rows' 1 / rms (residual form).  It comes from the previous kernel, so it is read only
+// after the accumulator wait, which follows the producer's wait for that kernel.
+__device__ __forceinline__ void qkv_row_scales(const GemmParams& p, QkvRows& q) {
+  if (!p.row_scale) return;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) q.rs[k] = __ldg(p.row_scale + min(q.m[k], p.M - 1));
 }
 
 // (cos, sin) of the 4 RoPE pairs a lane rotates in chunk-column block cc (0..3) of a head
@@ -374,6 +382,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[ab], (lt >> 1) & 1, abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();
+      if constexpr (EPI == kQkvRope) qkv_row_scales(p, qr);
       const uint32_t t_row = tmem_base + lane_off + ab * 256;
 #pragma unroll
       for (int cp = 0; cp < 4; ++cp) {
