@@ -166,3 +166,48 @@ def test_shard_chunked_prefill_and_large_decode_batch():
             shd.close()
     gu.assert_close(total, ref, what="chunked prefill, sum of 2 shard partials")
     gu.assert_close(total_d, ref_d, what="decode B=80, sum of 2 shard partials")
+
+
+@pytest.mark.parametrize("name", ["prefill_b1_t32768_tp8", "prefill_b1_t32768_tp2", "prefill_b1_t2048_tp8"])
+def test_shard_prefill_workloads_full_size_sampled_rows(name):
+    # one rank of the split as bench.py times it: kv groups 0 .. n-1 of the workload's
+    # weights, a cache of n groups; its partial Delta on sampled query rows against the
+    # oracle run with the same shard (4 n query heads, n kv heads)
+    w = gin.WORKLOADS[name]
+    inp = gin.make_inputs(name)
+    n = w.n_kv
+    sh = Shard(inp, 0, n)
+    try:
+        B, T = inp.x.shape[:2]
+        ck, cv = _shard_cache(B, T, n)
+        delta = torch.empty(B, T, 4096, dtype=torch.float32, device=gu.DEV)
+        abi.attn_prefill(sh.ctx, inp.x.to(gu.DEV), B, T, inp.R.to(gu.DEV), True, ck, cv, T, 0, delta)
+        abi.attn_sync_status(sh.ctx)
+        rows = gu.sample_rows(T)
+        w64 = [gin.to_f64(t) for t in tp.shard_weights(inp.wq, inp.wk, inp.wv, inp.wo, 0, n)]
+        ref, _ = orc.attention_block(gin.to_f64(inp.x), *w64, gin.to_f64(inp.R), rows=rows, n_heads=4 * n)
+        gu.assert_close(gu.np64(delta[:, rows]), ref, what=f"{name} partial delta rows")
+    finally:
+        sh.close()
+
+
+def test_shard_decode_workload_full_size_sampled_sequences():
+    name = "decode_b64_pos4095_tp8"
+    w = gin.WORKLOADS[name]
+    inp = gin.make_inputs(name)
+    n, pos = w.n_kv, w.start_pos
+    sh = Shard(inp, 0, n)
+    try:
+        ck = inp.cache_k[:, :, :n].contiguous().to(gu.DEV)
+        cv = inp.cache_v[:, :, :n].contiguous().to(gu.DEV)
+        d = torch.empty(w.B, 1, 4096, dtype=torch.float32, device=gu.DEV)
+        abi.attn_decode(sh.ctx, inp.x.to(gu.DEV), w.B, pos, inp.R.to(gu.DEV), ck, cv, w.s_max, d)
+        abi.attn_sync_status(sh.ctx)
+        w64 = [gin.to_f64(t) for t in tp.shard_weights(inp.wq, inp.wk, inp.wv, inp.wo, 0, n)]
+        for b in (0, 31, 63):
+            ref, _ = orc.attention_decode(gin.to_f64(inp.x[b:b + 1]), *w64, gin.to_f64(inp.R),
+                                          gin.to_f64(inp.cache_k[b:b + 1, :, :n]),
+                                          gin.to_f64(inp.cache_v[b:b + 1, :, :n]), pos, n_heads=4 * n)
+            gu.assert_close(gu.np64(d[b:b + 1]), ref, what=f"{name} partial delta, sequence {b}")
+    finally:
+        sh.close()
