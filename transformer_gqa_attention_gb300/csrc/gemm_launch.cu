@@ -6,8 +6,11 @@
 namespace gqa {
 
 using PairSmem = GemmPairSmem<6>;
-constexpr int kSkinnyStages = 8;  // one CTA per SM, 8 x 24 KB in flight
+constexpr int kSkinnyStages = 8;  // one CTA per SM, 8 x 24 KB in flight (64 token columns)
 using SkinnySmem = GemmSmem<64, kSkinnyStages>;
+// at most 32 tokens: a 4 KB activation stage, so 11 stages (176 KB of weights) are in flight
+constexpr int kNarrowStages = 11;
+using NarrowSmem = GemmSmem<32, kNarrowStages>;
 
 size_t gemm_wide_smem() { return PairSmem::kBytes; }
 size_t gemm_skinny_smem() { return SkinnySmem::kBytes; }
@@ -20,11 +23,17 @@ cudaError_t configure_gemm_kernels() {
   e = cudaFuncSetAttribute(gemm_tc_pair_kernel<6, kStoreF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            PairSmem::kBytes);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(gemm_splitk_cluster_kernel<kSplitKQkv, kSkinnyStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           SkinnySmem::kBytes);
+  e = cudaFuncSetAttribute(gemm_splitk_cluster_kernel<kSplitKQkv, kSkinnyStages, 64>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, SkinnySmem::kBytes);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemm_splitk_cluster_kernel<kSplitKOut, kSkinnyStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              SkinnySmem::kBytes);
+  e = cudaFuncSetAttribute(gemm_splitk_cluster_kernel<kSplitKOut, kSkinnyStages, 64>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, SkinnySmem::kBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(gemm_splitk_cluster_kernel<kSplitKQkv, kNarrowStages, 32>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, NarrowSmem::kBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemm_splitk_cluster_kernel<kSplitKOut, kNarrowStages, 32>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, NarrowSmem::kBytes);
 }
 
 int gemm_pair_max_clusters() {
@@ -51,11 +60,17 @@ cudaError_t launch_gemm_store_f32(const CUtensorMap& a, const CUtensorMap& b, co
 }
 
 // One cluster of p.splits CTAs per 128-feature tile (cluster rank = k split).
+// The activation map's box must be splitk_token_tile(p.N) rows.
 template <int EPI>
 static cudaError_t launch_splitk(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t s) {
-  return launch_pdl(gemm_splitk_cluster_kernel<EPI, kSkinnyStages>, dim3(p.m_tiles * p.splits), dim3(192),
+  if (p.N <= 32)
+    return launch_pdl(gemm_splitk_cluster_kernel<EPI, kNarrowStages, 32>, dim3(p.m_tiles * p.splits), dim3(192),
+                      NarrowSmem::kBytes, s, p.splits, a, b, p);
+  return launch_pdl(gemm_splitk_cluster_kernel<EPI, kSkinnyStages, 64>, dim3(p.m_tiles * p.splits), dim3(192),
                     SkinnySmem::kBytes, s, p.splits, a, b, p);
 }
+
+int splitk_token_tile(int n_tok) { return n_tok <= 32 ? 32 : 64; }
 
 cudaError_t launch_gemm_splitk_qkv(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int,
                                    cudaStream_t s) {

@@ -451,16 +451,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 //   kSplitKQkv — RoPE of Q and K pairs (adjacent lanes hold a pair), Q_r and the cache
 //                entries stored bf16 (steps 1-5);
 //   kSplitKOut — Delta stored fp32 (step 14).
-template <int EPI, int STAGES>
+// BN: token columns of the UMMA (64, or 32 for at most 32 tokens: a smaller activation stage,
+// so more weight stages fit in shared memory).
+template <int EPI, int STAGES, int BN>
 __global__ void __launch_bounds__(192, 1)
     gemm_splitk_cluster_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                                const GemmParams p) {
-  constexpr int BN = 64;
+  static_assert(BN == 32 || BN == 64, "token tile of 32 or 64");
   using L = GemmSmem<BN, STAGES>;
   // after the main loop the stage buffers hold this CTA's partial tile, token-major
   // [64 tokens][128 features] fp32, then the receive slots: per source rank the rows of the
-  // tokens this CTA reduces (at most 32 when splits >= 2)
-  constexpr int kRecvTokens = 32;
+  // tokens this CTA reduces (at most BN / 2 when splits >= 2)
+  constexpr int kRecvTokens = BN / 2;
   constexpr int kPartBytes = BN * 128 * 4;
   constexpr int kRecvSlotBytes = kRecvTokens * 128 * 4;
   static_assert(STAGES * L::kStageBytes >= kPartBytes + 8 * kRecvSlotBytes, "partials must fit in the stage buffers");

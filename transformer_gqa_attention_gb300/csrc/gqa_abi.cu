@@ -322,7 +322,7 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
   const int rows = c->qkv_rows();
   CUtensorMap ta, tb;
   if (sk) {
-    if (!map_weight_tiled(&ta, wqkv, rows, 64, 128) || !map_rows(&tb, x, n_tok, 4096, 64))
+    if (!map_weight_tiled(&ta, wqkv, rows, 64, 128) || !map_rows(&tb, x, n_tok, 4096, splitk_token_tile(n_tok)))
       return cuda_fail(cudaErrorInvalidValue);
     p.M = rows;
     p.N = n_tok;
@@ -368,7 +368,7 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
   p.num_kb = kc / 64;
   CUtensorMap ta, tb;
   if (sk) {
-    if (!map_weight_tiled(&ta, c->w_o, 4096, p.num_kb, 128) || !map_rows(&tb, h, n_tok, kc, 64))
+    if (!map_weight_tiled(&ta, c->w_o, 4096, p.num_kb, 128) || !map_rows(&tb, h, n_tok, kc, splitk_token_tile(n_tok)))
       return cuda_fail(cudaErrorInvalidValue);
     p.M = 4096;
     p.N = n_tok;

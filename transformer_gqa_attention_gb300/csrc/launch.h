@@ -61,7 +61,9 @@ cudaError_t launch_gemm_qkv_rope(const CUtensorMap& a, const CUtensorMap& b, con
                                  const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_gemm_store_f32(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bt,
                                   const GemmParams& p, int grid, cudaStream_t s);
-// Few-token split-K projections with the reduction fused (last split of each tile).
+// Few-token split-K projections with the reduction fused (last split of each tile).  The
+// activation tensor map's box holds splitk_token_tile(n_tok) rows.
+int splitk_token_tile(int n_tok);
 cudaError_t launch_gemm_splitk_qkv(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                                    int grid, cudaStream_t s);
 cudaError_t launch_gemm_splitk_out(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
