@@ -63,6 +63,8 @@ cudaError_t launch_gemm_store_f32(const CUtensorMap& a, const CUtensorMap& b, co
 // The activation map's box must be splitk_token_tile(p.N) rows.
 template <int EPI>
 static cudaError_t launch_splitk(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t s) {
+  // the reduction serves 2..8 splits (cluster sizes) of at most 64 tokens
+  if (p.splits < 2 || p.splits > 8 || p.N < 1 || p.N > 64) return cudaErrorInvalidValue;
   if (p.N <= 32)
     return launch_pdl(gemm_splitk_cluster_kernel<EPI, kNarrowStages, 32>, dim3(p.m_tiles * p.splits), dim3(192),
                       NarrowSmem::kBytes, s, p.splits, a, b, p);

@@ -516,6 +516,12 @@ __global__ void __launch_bounds__(192, 1)
   const int t_hi = (split + 1) * p.N / p.splits;
   if (threadIdx.x == 64)
     mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((p.splits - 1) * (t_hi - t_lo)) * 512u);
+  // Epilogue warp w reduces tokens t_lo + w + 4 j, j < kTokPerWarp (at most BN / 2 tokens per
+  // CTA for splits >= 2); for Q/K/V its lanes' RoPE coefficients of those tokens are read
+  // while the main loop runs (an input of the call), not one L2 round trip per token pair
+  // after the reduction
+  constexpr int kTokPerWarp = BN / 8;
+  float4 cs[kTokPerWarp];
 
   if (warp == 0) {
     if (lane == 0) {
@@ -572,6 +578,19 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
+    if constexpr (EPI == kSplitKQkv) {
+      const int m = m0 + 4 * lane;  // pairs (m & 127) / 2 and the next one
+      const bool rope = m < p.q_cols + p.kv_cols;
+#pragma unroll
+      for (int j = 0; j < kTokPerWarp; ++j) {
+        const int tok = t_lo + (warp - 2) + 4 * j;
+        cs[j] = make_float4(1.f, 0.f, 1.f, 0.f);  // value features: not rotated
+        if (rope && tok < t_hi) {
+          const int t = tok - (tok / p.T) * p.T;
+          cs[j] = __ldg(reinterpret_cast<const float4*>(p.R + (static_cast<size_t>(t) * 64 + ((m & 127) >> 1)) * 2));
+        }
+      }
+    }
     // accumulator rows (features) -> this CTA's partial tile in shared memory
     if (bar1_and_128(mbar_wait(acc_full, 0, abort_flag, p.status))) {
       tc_fence_after();
@@ -623,9 +642,10 @@ __global__ void __launch_bounds__(192, 1)
     const int ew = warp - 2;
     const int f0 = 4 * lane;
     const int m = m0 + f0;
-    const bool rope = EPI == kSplitKQkv && m < p.q_cols + p.kv_cols;
-#pragma unroll 2
-    for (int tok = t_lo + ew; tok < t_hi; tok += 4) {
+#pragma unroll
+    for (int j = 0; j < kTokPerWarp; ++j) {
+      const int tok = t_lo + ew + 4 * j;
+      if (tok >= t_hi) break;
       float4 acc = *reinterpret_cast<const float4*>(red + tok * 128 + f0);
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
@@ -651,11 +671,10 @@ __global__ void __launch_bounds__(192, 1)
         }
         const int b = tok / p.T;
         const int t = tok - b * p.T;
-        if (rope) {
-          // (cos, sin) of pairs (m & 127) / 2 and the next one
-          const float4 cs = __ldg(reinterpret_cast<const float4*>(p.R + (static_cast<size_t>(t) * 64 + ((m & 127) >> 1)) * 2));
+        if (m < p.q_cols + p.kv_cols) {  // RoPE of the Q and K pairs
+          const float4 c4 = cs[j];
           const float e0 = acc.x, o0 = acc.y, e1 = acc.z, o1 = acc.w;
-          acc = make_float4(cs.x * e0 - cs.y * o0, cs.y * e0 + cs.x * o0, cs.z * e1 - cs.w * o1, cs.w * e1 + cs.z * o1);
+          acc = make_float4(c4.x * e0 - c4.y * o0, c4.y * e0 + c4.x * o0, c4.z * e1 - c4.w * o1, c4.w * e1 + c4.z * o1);
         }
         const uint2 o = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
         if (m < p.q_cols) {
