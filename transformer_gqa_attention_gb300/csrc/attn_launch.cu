@@ -7,8 +7,6 @@ namespace gqa {
 
 cudaError_t configure_gemm_kernels();
 
-size_t flash_smem() { return FlashSmem::kBytes; }
-size_t decode_smem() { return DecodeSmemT<4>::kBytes; }
 
 cudaError_t configure_kernels() {
   cudaError_t e = configure_gemm_kernels();

@@ -12,8 +12,6 @@ using SkinnySmem = GemmSmem<64, kSkinnyStages>;
 constexpr int kNarrowStages = 11;
 using NarrowSmem = GemmSmem<32, kNarrowStages>;
 
-size_t gemm_wide_smem() { return PairSmem::kBytes; }
-size_t gemm_skinny_smem() { return SkinnySmem::kBytes; }
 
 cudaError_t configure_gemm_kernels() {
   cudaError_t e;
@@ -74,12 +72,12 @@ static cudaError_t launch_splitk(const CUtensorMap& a, const CUtensorMap& b, con
 
 int splitk_token_tile(int n_tok) { return n_tok <= 32 ? 32 : 64; }
 
-cudaError_t launch_gemm_splitk_qkv(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int,
+cudaError_t launch_gemm_splitk_qkv(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                                    cudaStream_t s) {
   return launch_splitk<kSplitKQkv>(a, b, p, s);
 }
 
-cudaError_t launch_gemm_splitk_out(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int,
+cudaError_t launch_gemm_splitk_out(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                                    cudaStream_t s) {
   return launch_splitk<kSplitKOut>(a, b, p, s);
 }

@@ -169,17 +169,15 @@ struct WsLayout {
   size_t q_off, h_off, dec_o_off, dec_ml_off, rstd_off, total;
 };
 
+// Few-token projections (at most kSkinnyMaxTokens tokens): k splits per 128-feature tile.
 struct SkinnyPlan {
-  int n_tiles, tok_pad, splits_qkv, splits_o;
+  int splits_qkv, splits_o;
 };
 
-SkinnyPlan skinny_plan(int n_tok, int num_sms) {
-  SkinnyPlan s;
-  s.n_tiles = (n_tok + 63) / 64;
-  s.tok_pad = s.n_tiles * 64;
+SkinnyPlan skinny_plan() {
   // k splits = cluster size, one CTA per SM; all clusters must be co-resident (GB300
   // holds 76 two-CTA or 36 four-CTA clusters of this kernel): 48 x 2 and 32 x 4 CTAs
-  (void)num_sms;
+  SkinnyPlan s;
   s.splits_qkv = 2;
   s.splits_o = 4;
   return s;
@@ -327,15 +325,14 @@ gqa_status run_qkv(gqa_ctx* c, const void* x, int n_tok, int T, const float* R, 
     p.M = rows;
     p.N = n_tok;
     p.splits = sk->splits_qkv;
-    p.n_tiles = sk->n_tiles;
+    p.n_tiles = 1;
     p.m_tiles = rows / 128;
     p.fin0 = q_out;
     p.fin1 = ck;
     p.fin2 = cv;
     p.R = R;
-    const int grid = std::min(p.m_tiles * p.n_tiles * p.splits, 2 * c->num_sms);
     p.fault = take_fault(c, GQA_KERNEL_QKV_SPLITK);
-    { ProfScope ps(c, GQA_KERNEL_QKV_SPLITK, s); GQA_CUDA(launch_gemm_splitk_qkv(ta, tb, p, grid, s)); }
+    { ProfScope ps(c, GQA_KERNEL_QKV_SPLITK, s); GQA_CUDA(launch_gemm_splitk_qkv(ta, tb, p, s)); }
   } else {
     // CTA pairs, 256x256 tiles: each CTA loads 128-row boxes of x and of W_QKV
     if (!map_rows(&ta, x, n_tok, 4096, 128) || !map_weight_tiled(&tb, wqkv, rows, 64, 128))
@@ -373,12 +370,11 @@ gqa_status run_out(gqa_ctx* c, const void* h, int n_tok, float* delta, const WsL
     p.M = 4096;
     p.N = n_tok;
     p.splits = sk->splits_o;
-    p.n_tiles = sk->n_tiles;
+    p.n_tiles = 1;
     p.m_tiles = 32;
     p.fin0 = delta;
-    const int grid = std::min(p.m_tiles * p.n_tiles * p.splits, 2 * c->num_sms);
     p.fault = take_fault(c, GQA_KERNEL_OUT_SPLITK);
-    { ProfScope ps(c, GQA_KERNEL_OUT_SPLITK, s); GQA_CUDA(launch_gemm_splitk_out(ta, tb, p, grid, s)); }
+    { ProfScope ps(c, GQA_KERNEL_OUT_SPLITK, s); GQA_CUDA(launch_gemm_splitk_out(ta, tb, p, s)); }
   } else {
     if (!map_rows(&ta, h, n_tok, kc, 128) || !map_weight_tiled(&tb, c->w_o, 4096, p.num_kb, 128))
       return cuda_fail(cudaErrorInvalidValue);
@@ -512,7 +508,7 @@ gqa_status prefill_impl(gqa_ctx* c, const void* x, int B, int T, const float* R,
   const int n_tok = B * T;
   const int G = c->n_kv;
   const int kv_len = start_pos + T;
-  SkinnyPlan sk_v = skinny_plan(n_tok, c->num_sms);
+  SkinnyPlan sk_v = skinny_plan();
   const SkinnyPlan* sk = n_tok <= kSkinnyMaxTokens ? &sk_v : nullptr;
   // few positions per sequence: the decode attention kernel, 4 positions per CTA
   const int n_pg = (T + kShortPos - 1) / kShortPos;
@@ -621,7 +617,7 @@ gqa_status decode_impl(gqa_ctx* c, const void* x, int B, int start_pos, const fl
 
   const int kv_len = start_pos + 1;
   const int G = c->n_kv;
-  SkinnyPlan sk_v = skinny_plan(B, c->num_sms);
+  SkinnyPlan sk_v = skinny_plan();
   const SkinnyPlan* sk = B <= kSkinnyMaxTokens ? &sk_v : nullptr;
   const DecodePlan dp = decode_plan(B, G, kv_len, c->num_sms);
   const WsLayout w = ws_layout(B, G, sk, &dp, static_cast<long long>(B) * 4);

@@ -43,12 +43,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // translation unit of the library reports through it).
 void set_last_cuda_error(cudaError_t e);
 
-// Dynamic shared memory each kernel needs (bytes).
-size_t gemm_wide_smem();    // 128x256 tiles (prefill)
-size_t gemm_skinny_smem();  // 128x64 tiles (few tokens, split-K)
-size_t flash_smem();
-size_t decode_smem();
-
 // One-time per-process opt-in to large dynamic shared memory on the current device.
 cudaError_t configure_kernels();
 
@@ -64,10 +58,11 @@ cudaError_t launch_gemm_store_f32(const CUtensorMap& a, const CUtensorMap& b, co
 // Few-token split-K projections with the reduction fused (last split of each tile).  The
 // activation tensor map's box holds splitk_token_tile(n_tok) rows.
 int splitk_token_tile(int n_tok);
+// One cluster of p.splits CTAs (2..8) per 128-feature tile, at most 64 tokens.
 cudaError_t launch_gemm_splitk_qkv(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                                   int grid, cudaStream_t s);
+                                   cudaStream_t s);
 cudaError_t launch_gemm_splitk_out(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                                   int grid, cudaStream_t s);
+                                   cudaStream_t s);
 
 cudaError_t launch_flash_prefill(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                  const CUtensorMap& h, const FlashParams& p, dim3 grid, cudaStream_t s);

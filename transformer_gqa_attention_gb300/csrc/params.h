@@ -21,7 +21,7 @@ struct GemmParams {
   int M, N;          // rows of A, rows of B
   int num_kb;        // K / 64
   int splits;        // few-token kernel: k splits = cluster size
-  int n_tiles;       // ceil(N / BN)
+  int n_tiles;       // CTA-pair kernels: 256-wide output tiles along N (split-K kernels: 1)
   int m_tiles;       // ceil(M / 128)
   // CTA-pair kernel schedule: full_rounds rounds of whole 256x256 tiles, then the tiles of
   // the last, partial round cut into pieces of tail_w columns (0: whole tiles throughout)
