@@ -1,4 +1,5 @@
-"""Seeded sweep over the prefill parameter space through the C ABI against the fp64 oracle.
+"""Seeded sweeps over the prefill and decode parameter spaces through the C ABI against the
+fp64 oracle.
 
 Each case draws (B, T, start_pos, causal, kv-group shard) at random from one seeded
 generator: a context over kv groups g0 .. g0+n-1 (the whole block when n = 8) fills its cache
@@ -76,5 +77,42 @@ def test_prefill_sweep(i, B, T, start_pos, causal, g0, n):
                                          n_heads=4 * n)
         gu.assert_close(gu.np64(d), ref,
                         what=f"case {i}: B={B} T={T} start_pos={start_pos} causal={causal} groups {g0}+{n}")
+    finally:
+        abi.attn_destroy(ctx)
+
+
+def _decode_cases():
+    rng = np.random.default_rng(2025)
+    out = []
+    for i in range(12):
+        n = int(rng.choice([8, 8, 4, 1]))
+        g0 = int(rng.integers(0, 8 // n)) * n
+        B = int(rng.choice([1, 5, 32, 33, 64, 80]))
+        pos = int(rng.choice([0, 1, 63, 64, 500, 2100]))
+        out.append((i, B, pos, g0, n))
+    return out
+
+
+@pytest.mark.parametrize("i,B,pos,g0,n", _decode_cases())
+def test_decode_sweep(i, B, pos, g0, n):
+    # one decode step at position pos against a cache holding positions < pos (drawn): the
+    # batch crosses the 32-token and 64-token projection kernels and the many-token path
+    # (B = 80), the cache length crosses the 64-key tile and several key splits
+    S_max = pos + 1
+    inp = gin.make_custom(seed=600 + i, B=B, T=1, start_pos=pos, S_max=S_max, fill_cache=True)
+    ws = tp.shard_weights(inp.wq, inp.wk, inp.wv, inp.wo, g0, n)
+    wd = [t.to(gu.DEV) for t in ws]
+    ctx = abi.attn_create(*wd) if n == 8 else abi.attn_create_shard(*wd, n)
+    try:
+        ck = inp.cache_k[:, :, g0:g0 + n].contiguous().to(gu.DEV)
+        cv = inp.cache_v[:, :, g0:g0 + n].contiguous().to(gu.DEV)
+        d = torch.empty(B, 1, 4096, dtype=torch.float32, device=gu.DEV)
+        abi.attn_decode(ctx, inp.x.to(gu.DEV), B, pos, inp.R.to(gu.DEV), ck, cv, S_max, d)
+        abi.attn_sync_status(ctx)
+        w64 = [gin.to_f64(t) for t in ws]
+        ref, _ = orc.attention_decode(gin.to_f64(inp.x), *w64, gin.to_f64(inp.R),
+                                      gin.to_f64(inp.cache_k[:, :, g0:g0 + n]),
+                                      gin.to_f64(inp.cache_v[:, :, g0:g0 + n]), pos, n_heads=4 * n)
+        gu.assert_close(gu.np64(d), ref, what=f"decode case {i}: B={B} pos={pos} groups {g0}+{n}")
     finally:
         abi.attn_destroy(ctx)
