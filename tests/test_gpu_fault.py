@@ -70,3 +70,31 @@ def test_decode_timeout_reported_and_context_recovers(kind):
         gu.assert_close(gu.np64(delta), ref, what=f"after {kind} timeout")
     finally:
         blk.close()
+
+
+@pytest.mark.parametrize("start_pos", [0, 1265])
+def test_short_prefill_timeout_reported_and_context_recovers(start_pos):
+    # T = 16 runs the four-position attention kernel: with one key split (start_pos 0) an
+    # aborted CTA writes no H; with five splits (a 1281-key cache) its split never arrives, so
+    # its group's arrival counter stays short until attn_sync_status resets the counters
+    B, T = 1, 16
+    full = gin.make_custom(seed=73 + start_pos, B=B, T=start_pos + T)
+    blk = gu.Block(full)
+    try:
+        S_max = start_pos + T
+        ck, cv = gu.empty_cache(B, S_max)
+        x, R = full.x.to(gu.DEV), full.R.to(gu.DEV)
+        if start_pos:
+            blk.prefill(x[:, :start_pos].contiguous(), R[:start_pos].contiguous(), ck, cv)
+        xs, Rs = x[:, start_pos:].contiguous(), R[start_pos:].contiguous()
+        delta = torch.empty(B, T, 4096, dtype=torch.float32, device=gu.DEV)
+        abi.attn_debug_inject_timeout(blk.ctx, "decode_attn")
+        abi.attn_prefill(blk.ctx, xs, B, T, Rs, True, ck, cv, S_max, start_pos, delta)
+        with pytest.raises(abi.GQAError) as err:
+            abi.attn_sync_status(blk.ctx)
+        assert err.value.status == 5
+        d = blk.prefill(xs, Rs, ck, cv, start_pos=start_pos)
+        ref, _ = gu.oracle_prefill(blk, full, rows=list(range(start_pos, start_pos + T)))
+        gu.assert_close(gu.np64(d), ref, what=f"short prefill after a timeout (start_pos {start_pos})")
+    finally:
+        blk.close()
