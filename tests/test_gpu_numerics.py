@@ -4,7 +4,9 @@ Scaling W_Q changes only how peaked the softmax is: x3 makes the scores ~3 times
 ~7 in log2 units), so each row is dominated by a few keys; W_Q = 0 makes every visible key
 equally likely, so H is the running mean of V (a closed form).  Each case runs the flash
 kernel (several tiles, a ragged tail), the four-position short-prefill kernel or the decode
-kernel, and compares with the fp64 oracle.
+kernel, and compares with the fp64 oracle.  Spikes (one token's x, or one cached key and
+value, scaled 20x) make row maxima jump past the lazy-rescale threshold in a later key tile and
+make one key split dominate the split merge.
 
 Peaked scores amplify the rounding of the bf16 intermediates (Q_r, K_r, V, P, H): a score
 error of |S| 2^-9 becomes a relative error of P.  The bound for these cases is therefore
@@ -117,5 +119,57 @@ def test_decode_softmax_extremes(factor):
         rl1, rmx = _bound(_floor_delta(ex["Q_r"], ex["cache_k"][:, :pos + 1], ex["cache_v"][:, :pos + 1], wo, pos),
                           ref)
         gu.assert_close(gu.np64(d), ref, rl1, rmx, what=f"decode, W_Q x{factor} (bound {rl1:.2e} / {rmx:.2e})")
+    finally:
+        blk.close()
+
+
+def _spike(t, index, factor=20.0):
+    t = t.clone()
+    t[index] = (t[index].float() * factor).to(torch.bfloat16)
+    return t
+
+
+def test_spike_key_forces_rescale_prefill():
+    # token 200's x scaled 20x: its key dominates (or vanishes from) every later row, so the
+    # running max of many rows jumps far past the lazy-rescale threshold in the second 128-key
+    # tile, and its value dominates those rows' H
+    T = 600
+    inp = gin.make_custom(seed=730, B=1, T=T)
+    inp.x = _spike(inp.x, (0, 200))
+    blk = gu.Block(inp)
+    try:
+        ck, cv = gu.empty_cache(1, T)
+        delta = blk.prefill(inp.x.to(gu.DEV), inp.R.to(gu.DEV), ck, cv)
+        ref, ex = gu.oracle_prefill(blk, inp, keep=True)
+        rl1, rmx = _bound(_floor_delta(ex["Q_r"], ex["K_r"], ex["V"], blk.w64[3], 0), ref)
+        gu.assert_close(gu.np64(delta), ref, rl1, rmx, what=f"spike key, T={T} (bound {rl1:.2e} / {rmx:.2e})")
+    finally:
+        blk.close()
+
+
+@pytest.mark.parametrize("T", [1, 16])
+def test_spike_key_across_key_splits(T):
+    # a cache of 1281 positions (several key splits) whose position 700 has a 20x key and
+    # value: the split holding it has a running max far above the others', so the split merge
+    # (log-sum-exp) must weight the other splits by ~0; T = 1 is the decode kernel, T = 16 the
+    # four-position kernel (a prefill continuing the cache)
+    B, start_pos = 2, 1281 - T
+    S_max = start_pos + T
+    inp = gin.make_custom(seed=740 + T, B=B, T=T, start_pos=start_pos, S_max=S_max, fill_cache=True)
+    inp.cache_k = _spike(inp.cache_k, (slice(None), 700))
+    inp.cache_v = _spike(inp.cache_v, (slice(None), 700))
+    blk = gu.Block(inp)
+    try:
+        ck, cv = inp.cache_k.to(gu.DEV), inp.cache_v.to(gu.DEV)
+        if T == 1:
+            d = blk.decode(inp.x.to(gu.DEV), inp.R.to(gu.DEV), ck, cv, start_pos)
+        else:
+            d = blk.prefill(inp.x.to(gu.DEV), inp.R.to(gu.DEV), ck, cv, start_pos=start_pos)
+        wq, wk, wv, wo = blk.w64
+        ref, ex = orc.attention_block(gin.to_f64(inp.x), wq, wk, wv, wo, gin.to_f64(inp.R), start_pos=start_pos,
+                                      cache_k=gin.to_f64(inp.cache_k), cache_v=gin.to_f64(inp.cache_v), keep=True)
+        rl1, rmx = _bound(_floor_delta(ex["Q_r"], ex["cache_k"][:, :S_max], ex["cache_v"][:, :S_max], wo, start_pos),
+                          ref)
+        gu.assert_close(gu.np64(d), ref, rl1, rmx, what=f"spike in a long cache, T={T} (bound {rl1:.2e} / {rmx:.2e})")
     finally:
         blk.close()
