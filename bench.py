@@ -214,10 +214,15 @@ def oracle_sample_step(inp, w: gin.Workload, n_tokens: int, seqs: int, w64):
     if w.kind == "prefill":
         x = gin.to_f64(inp.x[:seqs, :n_tokens])
         R = gin.to_f64(inp.R[:n_tokens])
+        kw = {}
+        if w.start_pos:  # a chunk continuing a cache: its first n_tokens rows against it
+            n_keys = w.start_pos + n_tokens
+            kw = dict(start_pos=w.start_pos, cache_k=gin.to_f64(inp.cache_k[:seqs, :n_keys]),
+                      cache_v=gin.to_f64(inp.cache_v[:seqs, :n_keys]))
         if w.residual:
-            orc.attention_block_residual(x, wn, wq, wk, wv, wo, R, causal=w.causal)
+            orc.attention_block_residual(x, wn, wq, wk, wv, wo, R, causal=w.causal, **kw)
         else:
-            orc.attention_block(x, wq, wk, wv, wo, R, causal=w.causal)
+            orc.attention_block(x, wq, wk, wv, wo, R, causal=w.causal, **kw)
         units = seqs * n_tokens
     else:
         pos = w.start_pos
@@ -414,8 +419,12 @@ def measure_gpu(args, w: gin.Workload, inp, world, rank, local, steps, warmup):
     x = inp.x.to(dev)
     R = inp.R.to(dev)
     if w.kind == "prefill":
-        ck = torch.zeros(B, S_max, G, 128, dtype=torch.bfloat16, device=dev)
-        cv = torch.zeros_like(ck)
+        if inp.cache_k is not None:  # a chunk continuing a drawn cache
+            ck = inp.cache_k[:, :, :G].contiguous().to(dev)
+            cv = inp.cache_v[:, :, :G].contiguous().to(dev)
+        else:
+            ck = torch.zeros(B, S_max, G, 128, dtype=torch.bfloat16, device=dev)
+            cv = torch.zeros_like(ck)
         delta = torch.empty(B, T, 4096, dtype=torch.float32, device=dev)
         fn = abi.attn_prefill_residual if w.residual else abi.attn_prefill
 

@@ -74,3 +74,17 @@ def test_shard_accounting_is_the_whole_divided_by_the_split():
     w = gin.WORKLOADS["prefill_b1_t2048_tp8"]
     assert bench.kernel_work("qkv_gemm", w)[1] == 2.0 * 2048 * 4096 * 768
     assert bench.kernel_work("out_gemm", w)[1] == 2.0 * 2048 * 512 * 4096
+
+
+def test_chunked_prefill_workloads_accounting():
+    # the last 2048-token chunk of a 32768-token prompt: each row t sees 30720 + t + 1 keys
+    w = gin.WORKLOADS["prefill_b1_t2048_pos30720"]
+    proj, attn = bench.prefill_flops(w.B, w.T, w.start_pos, w.causal)
+    assert proj == 2 * 41_943_040 * 2048
+    assert attn == 4 * 128 * 32 * sum(30720 + t + 1 for t in range(2048))
+    # 16 tokens after 4080 cached positions run the four-position kernel: K and V of all 4096
+    # positions of the 4 sequences once, q in and H out
+    s = gin.WORKLOADS["prefill_b4_t16_pos4080"]
+    assert bench.kernel_work("decode_attn", s)[1] == float(4 * 4096 * 8 * 128 * 4 + 2 * 64 * 4096 * 2)
+    inp = gin.make_inputs(s)
+    assert inp.cache_k.shape == (4, 4096, 8, 128) and inp.R.shape == (16, 64, 2)

@@ -153,7 +153,7 @@ def test_spike_key_across_key_splits(T):
     # value: the split holding it has a running max far above the others', so the split merge
     # (log-sum-exp) must weight the other splits by ~0; T = 1 is the decode kernel, T = 16 the
     # four-position kernel (a prefill continuing the cache)
-    B, start_pos = 2, 1281 - T
+    B, start_pos = (2, 1280) if T == 1 else (1, 1265)  # B = 1: the 16 positions take the four-position kernel
     S_max = start_pos + T
     inp = gin.make_custom(seed=740 + T, B=B, T=T, start_pos=start_pos, S_max=S_max, fill_cache=True)
     inp.cache_k = _spike(inp.cache_k, (slice(None), 700))

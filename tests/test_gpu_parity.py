@@ -327,3 +327,28 @@ def test_causality_and_determinism_bit_exact():
         assert not torch.equal(d2[:, t0 + 1:], d0[:, t0 + 1:])
     finally:
         blk.close()
+
+
+@pytest.mark.parametrize("name", ["prefill_b1_t2048_pos30720", "prefill_b4_t16_pos4080"])
+def test_prefill_continuing_a_drawn_cache_workloads(name):
+    # the chunked-prefill workloads as bench.py times them: a drawn cache of start_pos
+    # positions, the chunk's rows (sampled for the long chunk) against the oracle with that cache
+    w = gin.WORKLOADS[name]
+    inp = gin.make_inputs(name)
+    blk = gu.Block(inp)
+    try:
+        B, T = inp.x.shape[:2]
+        ck, cv = inp.cache_k.to(gu.DEV), inp.cache_v.to(gu.DEV)
+        delta = blk.prefill(inp.x.to(gu.DEV), inp.R.to(gu.DEV), ck, cv, start_pos=w.start_pos)
+        rows = gu.sample_rows(T) if T > 64 else np.arange(T)
+        wq, wk, wv, wo = blk.w64
+        ref, ex = orc.attention_block(gin.to_f64(inp.x), wq, wk, wv, wo, gin.to_f64(inp.R), start_pos=w.start_pos,
+                                      cache_k=gin.to_f64(inp.cache_k), cache_v=gin.to_f64(inp.cache_v), rows=rows)
+        gu.assert_close(gu.np64(delta[:, rows]), ref, what=f"{name} delta rows")
+        # the chunk's keys and values landed after the cached positions, the cache before is intact
+        n_keys = w.start_pos + T
+        gu.assert_close(gu.np64(ck[:, w.start_pos:n_keys]), ex["cache_k"][:, w.start_pos:n_keys],
+                        gu.TOL_BF16_REL_L1, gu.TOL_BF16_MAX, "chunk K_r in the cache")
+        np.testing.assert_array_equal(gu.np64(ck[:, :w.start_pos]), gin.to_f64(inp.cache_k[:, :w.start_pos]))
+    finally:
+        blk.close()

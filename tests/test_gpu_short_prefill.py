@@ -6,12 +6,15 @@ Cases: every position-group shape (T = 1 .. 16, ragged groups of 1-3 positions),
 continuing caches across the 64-key tile and over several key splits (including a split that
 holds no visible key for the first position group), the non-causal form, the largest batch
 the arrival counters serve (256 sequences x 16 positions) and the first batch past it (257,
-which falls back to the flash kernel)."""
+which falls back to the flash kernel), and which kernel a call runs: the four-position kernel
+while the cache is at most 256 keys or the flash grid would have fewer than 32 CTAs, else the
+flash kernel (its tcgen05 tiles cost less per key once its grid fills the GPU)."""
 import numpy as np
 import pytest
 import torch
 
 from tests import gpu_util as gu
+from transformer_gqa_attention_gb300 import abi
 from transformer_gqa_attention_gb300 import inputs as gin
 
 pytestmark = pytest.mark.gpu
@@ -70,12 +73,37 @@ def _continue_cache(B, T, start_pos, seed, causal=True):
         blk.close()
 
 
-@pytest.mark.parametrize("B,T,start_pos", [(2, 16, 48), (2, 5, 60), (3, 16, 1000), (1, 13, 4090),
-                                           (1, 16, 1265), (2, 9, 127)])
+@pytest.mark.parametrize("B,T,start_pos", [(2, 16, 48), (2, 5, 60), (1, 16, 1000), (1, 13, 4090),
+                                           (1, 16, 1265), (2, 9, 127), (3, 16, 1000)])
 def test_short_prefill_continuing_a_cache(B, T, start_pos):
     # (16, 48): the chunk ends on the 64-key tile; (5, 60): it straddles it; (13, 4090):
-    # several key splits; (16, 1265): the first position group sees no key of the last split
+    # several key splits; (16, 1265): the first position group sees no key of the last split;
+    # (3, 16, 1000): a long cache with a batch whose flash grid fills the GPU: the flash kernel
     _continue_cache(B, T, start_pos, seed=330 + T + start_pos)
+
+
+@pytest.mark.parametrize("B,T,start_pos,kernel", [(1, 16, 0, "decode_attn"), (4, 16, 0, "decode_attn"),
+                                                  (4, 16, 240, "decode_attn"), (1, 16, 4080, "decode_attn"),
+                                                  (2, 16, 4080, "flash_prefill"), (4, 16, 496, "flash_prefill"),
+                                                  (1, 17, 0, "flash_prefill")])
+def test_kernel_choice_for_short_prefills(B, T, start_pos, kernel):
+    # which attention kernel a call runs (the library's per-kernel profile): the four-position
+    # kernel up to 16 positions while the cache is short or the flash grid would be small
+    inp = gin.make_custom(seed=360, B=B, T=start_pos + T)
+    blk = gu.Block(inp)
+    try:
+        S_max = start_pos + T
+        ck, cv = gu.empty_cache(B, S_max)
+        x, R = inp.x.to(gu.DEV), inp.R.to(gu.DEV)
+        if start_pos:
+            blk.prefill(x[:, :start_pos].contiguous(), R[:start_pos].contiguous(), ck, cv)
+        abi.attn_profile_begin(blk.ctx)
+        blk.prefill(x[:, start_pos:].contiguous(), R[start_pos:].contiguous(), ck, cv, start_pos=start_pos)
+        prof = abi.attn_profile_end(blk.ctx)
+        ran = {k for k, (_, n) in prof.items() if n > 0 and k in ("decode_attn", "flash_prefill")}
+        assert ran == {kernel}, prof
+    finally:
+        blk.close()
 
 
 def test_non_causal_chunk_sees_the_whole_cache():

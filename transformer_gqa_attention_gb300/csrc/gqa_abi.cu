@@ -80,9 +80,16 @@ constexpr int kDecodeMaxBatch = 1024;
 constexpr int kCounterInts = kDecodeMaxBatch * 8;
 // Prefills of at most this many tokens per sequence run the decode attention kernel with
 // kShortPos positions per CTA instead of the flash kernel (whose 128-row query tiles they
-// would fill to an eighth at most).
+// would fill to an eighth at most) — unless the cache is long and the flash grid fills the
+// GPU: each position group of the short kernel reads the keys again, and its mma.sync rows
+// cost more per key than the flash kernel's tcgen05 tiles.  Measured block steps at T = 16:
+// B = 1 is faster on the short kernel up to 4096 cached keys (61 vs 76 us); B = 2 ties at
+// 1024 keys and loses at 4096 (81 vs 77 us); B = 4 wins up to 256 keys and loses from 512
+// (54 vs 44 us; at 4096 97 vs 79 us).
 constexpr int kShortMaxT = 16;
 constexpr int kShortPos = 4;
+constexpr int kShortAlwaysKeys = 256;     // at most this many keys: the short kernel
+constexpr int kFlashMinCtas = 32;         // longer caches: flash once its grid has this many CTAs
 
 // ------------------------------------------------------------------ tensor maps
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -512,7 +519,8 @@ gqa_status prefill_impl(gqa_ctx* c, const void* x, int B, int T, const float* R,
   const SkinnyPlan* sk = n_tok <= kSkinnyMaxTokens ? &sk_v : nullptr;
   // few positions per sequence: the decode attention kernel, 4 positions per CTA
   const int n_pg = (T + kShortPos - 1) / kShortPos;
-  const bool short_path = T <= kShortMaxT && static_cast<long long>(B) * G * n_pg <= kCounterInts;
+  const bool short_path = T <= kShortMaxT && static_cast<long long>(B) * G * n_pg <= kCounterInts &&
+                          (kv_len <= kShortAlwaysKeys || 2LL * G * B < kFlashMinCtas);
   const DecodePlan dp = decode_plan(B * n_pg, G, kv_len, c->num_sms, 1);
   const WsLayout w = short_path ? ws_layout(n_tok, G, sk, &dp, static_cast<long long>(B) * n_pg * 4 * kShortPos)
                                 : ws_layout(n_tok, G, sk, nullptr, 0);

@@ -57,7 +57,8 @@ class Workload:
 
 
 # The workloads the block is measured and checked on: the five shapes of the block itself,
-# then two of them through the residual form.
+# then two of them through the residual form, shards of a head split, and prefills that
+# continue a cache.
 WORKLOADS = {
     w.name: w
     for w in [
@@ -77,6 +78,11 @@ WORKLOADS = {
         Workload("prefill_b1_t32768_tp2", "prefill", B=1, T=32768, seed=4, n_kv=4),
         Workload("prefill_b1_t2048_tp8", "prefill", B=1, T=2048, seed=1, n_kv=1),
         Workload("decode_b64_pos4095_tp8", "decode", B=64, T=1, seed=3, start_pos=4095, S_max=4096, n_kv=1),
+        # prefills continuing a cache (chunked prefill): the last 2048-token chunk of a
+        # 32768-token prompt, and 16 new tokens of 4 sequences after 4080 cached positions
+        # (e.g. verifying drafted tokens); the cached positions are drawn like a decode cache
+        Workload("prefill_b1_t2048_pos30720", "prefill", B=1, T=2048, seed=5, start_pos=30720, S_max=32768),
+        Workload("prefill_b4_t16_pos4080", "prefill", B=4, T=16, seed=6, start_pos=4080, S_max=4096),
     ]
 }
 
@@ -162,7 +168,7 @@ def make_inputs(w: Workload | str, *, T: int | None = None, B: int | None = None
     wq, wk, wv, wo = make_weights(gen)
     cache_k = cache_v = None
     s_max = w.S_max if w.S_max else w.start_pos + Tv
-    if w.kind == "decode":
+    if w.kind == "decode" or w.start_pos > 0:
         cache_k = _draw(gen, (Bv, s_max, N_KV_HEADS, HEAD_DIM), CACHE_STD)
         cache_v = _draw(gen, (Bv, s_max, N_KV_HEADS, HEAD_DIM), CACHE_STD)
     R = rope_table(np.arange(w.start_pos, w.start_pos + Tv))
