@@ -44,6 +44,13 @@ struct GemmSmem {
   static constexpr int kBytes = kBarOffset + 256 + 1024;  // + barriers + alignment slack
 };
 
+// Few-token split-K kernel: whether the partial tile [BN][128] fp32 and the receive slots
+// (splits x ceil(BN / splits) token rows of 512 bytes) fit in the STAGES stage buffers.
+template <int BN, int STAGES>
+constexpr bool splitk_fits(int splits) {
+  return BN * 128 * 4 + splits * ((BN + splits - 1) / splits) * 512 <= STAGES * GemmSmem<BN, STAGES>::kStageBytes;
+}
+
 // Epilogue of 32 x 32 chunks held by a warp (lane i = output row m_base + i).  A chunk goes
 // through a per-warp shared-memory tile (32 rows, stride 36 floats: conflict-free 16-byte
 // writes and reads) so that global stores and the RoPE table reads cover contiguous row
@@ -454,18 +461,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 // BN: token columns of the UMMA (64, or 32 for at most 32 tokens: a smaller activation stage,
 // so more weight stages fit in shared memory).
 template <int EPI, int STAGES, int BN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, (STAGES <= 5 ? 2 : 1))
     gemm_splitk_cluster_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                                const GemmParams p) {
   static_assert(BN == 32 || BN == 64, "token tile of 32 or 64");
   using L = GemmSmem<BN, STAGES>;
   // after the main loop the stage buffers hold this CTA's partial tile, token-major
-  // [64 tokens][128 features] fp32, then the receive slots: per source rank the rows of the
-  // tokens this CTA reduces (at most BN / 2 when splits >= 2)
-  constexpr int kRecvTokens = BN / 2;
+  // [BN tokens][128 features] fp32, then the receive slots: per source rank the rows of the
+  // tokens this CTA reduces, slot_tok = ceil(BN / splits) of them (splitk_fits checks on the
+  // host that partial tile and slots fit in the stage buffers)
   constexpr int kPartBytes = BN * 128 * 4;
-  constexpr int kRecvSlotBytes = kRecvTokens * 128 * 4;
-  static_assert(STAGES * L::kStageBytes >= kPartBytes + 8 * kRecvSlotBytes, "partials must fit in the stage buffers");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -473,7 +478,7 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * L::kABytes;
   float* red = reinterpret_cast<float*>(smem);                // [64 tokens][128] partial tile
-  float* recv = reinterpret_cast<float*>(smem + kPartBytes);  // [source rank][kRecvTokens][128]
+  float* recv = reinterpret_cast<float*>(smem + kPartBytes);  // [source rank][slot_tok][128]
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* acc_full = empty_bar + STAGES;
@@ -514,6 +519,7 @@ __global__ void __launch_bounds__(192, 1)
   // from every other split
   const int t_lo = split * p.N / p.splits;
   const int t_hi = (split + 1) * p.N / p.splits;
+  const int slot_tok = (BN + p.splits - 1) / p.splits;
   if (threadIdx.x == 64)
     mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((p.splits - 1) * (t_hi - t_lo)) * 512u);
   // Epilogue warp w reduces tokens t_lo + w + 4 j, j < kTokPerWarp (at most BN / 2 tokens per
@@ -620,7 +626,7 @@ __global__ void __launch_bounds__(192, 1)
       const int d_lo = d * p.N / p.splits;
       const int d_hi = (d + 1) * p.N / p.splits;
       if (d == split || d_hi == d_lo) continue;
-      bulk_copy_smem_to_cluster(mapa_shared(smem_u32(recv) + split * kRecvSlotBytes, d),
+      bulk_copy_smem_to_cluster(mapa_shared(smem_u32(recv) + static_cast<uint32_t>(split * slot_tok) * 512u, d),
                                 smem_u32(red + d_lo * 128), static_cast<uint32_t>(d_hi - d_lo) * 512u,
                                 mapa_shared(smem_u32(recv_bar), d));
     }
@@ -650,7 +656,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
         if (r < p.splits && r != split) {
-          const float4 v = *reinterpret_cast<const float4*>(recv + (r * kRecvTokens + tok - t_lo) * 128 + f0);
+          const float4 v = *reinterpret_cast<const float4*>(recv + (r * slot_tok + tok - t_lo) * 128 + f0);
           acc.x += v.x;
           acc.y += v.y;
           acc.z += v.z;
