@@ -99,16 +99,40 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without comments and blank lines (string literals are kept)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':  # string literal, copied as is
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def source_digest():
-    """Digest of the CUDA/C++ sources of the library (the kernels the ncu figures describe)."""
+    """Digest of the CUDA/C++ code of the library (the kernels the ncu figures describe);
+    comments and blank lines do not count."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "transformer_gqa_attention_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if not f.endswith((".cu", ".cuh", ".h")):
             continue
-        with open(os.path.join(csrc, f), "rb") as fh:
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             h.update(f.encode())
-            h.update(fh.read())
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

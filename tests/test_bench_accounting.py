@@ -88,3 +88,10 @@ def test_chunked_prefill_workloads_accounting():
     assert bench.kernel_work("decode_attn", s)[1] == float(4 * 4096 * 8 * 128 * 4 + 2 * 64 * 4096 * 2)
     inp = gin.make_inputs(s)
     assert inp.cache_k.shape == (4, 4096, 8, 128) and inp.R.shape == (16, 64, 2)
+
+
+def test_source_digest_ignores_comments_only():
+    code = 'int f(int a) {  // add one\n  return a + 1;  /* done */\n}\nconst char* s = "// kept";\n'
+    assert bench._code_only(code) == bench._code_only(code.replace("add one", "increment").replace("done", "ok") + "\n\n")
+    assert bench._code_only(code) != bench._code_only(code.replace("a + 1", "a + 2"))
+    assert '"// kept"' in bench._code_only(code)

@@ -13,7 +13,7 @@
 //     with the reduction done through distributed shared memory.
 //
 // Operands are read through 3-D tensor maps (64 columns, rows, 64-column k block), box
-// 64 x {64,128} x 1 (and 64 x tail_w/2 x 1 for the weight rows of a last-round piece), so
+// 64 x {32,64,128} x 1 (and 64 x tail_w/2 x 1 for the weight rows of a last-round piece), so
 // the same kernels read row-major activations (k-block stride 128 B) and the k-block-major
 // weight copies the context keeps (each 128-row box one contiguous 16 KB).
 //
@@ -452,14 +452,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 // Few-token projections (swap-AB: A = 128 weight rows = output features, B = the <= 64
 // token rows), split along K over the CTAs of one thread-block cluster (cluster rank =
 // split).  Each CTA accumulates its K range in TMEM, parks the fp32 partial tile
-// [64 tokens][128 features] in its own shared memory, and after one cluster barrier reduces
-// its share of the tokens by reading the partial tiles of all CTAs of the cluster
-// (distributed shared memory), then applies the final epilogue:
+// [BN tokens][128 features] in its own shared memory, and after one cluster barrier pushes
+// to each peer, with one bulk shared-to-shared copy, the rows of the tokens that peer
+// reduces; each CTA then sums its own tokens from its shared memory and applies the final
+// epilogue:
 //   kSplitKQkv — RoPE of Q and K pairs (adjacent lanes hold a pair), Q_r and the cache
 //                entries stored bf16 (steps 1-5);
 //   kSplitKOut — Delta stored fp32 (step 14).
-// BN: token columns of the UMMA (64, or 32 for at most 32 tokens: a smaller activation stage,
-// so more weight stages fit in shared memory).
+// BN: token columns of the UMMA (64, or 32 for at most 32 tokens: a smaller activation
+// stage).  STAGES <= 5 runs two CTAs per SM: a CTA's loop is bound by the tensor core's cost
+// per 128 x BN x 16 instruction rather than by bytes in flight, so two CTAs over shorter k
+// ranges finish sooner than one with a deeper ring.
 template <int EPI, int STAGES, int BN>
 __global__ void __launch_bounds__(192, (STAGES <= 5 ? 2 : 1))
     gemm_splitk_cluster_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
