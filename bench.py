@@ -9,8 +9,9 @@ HBM.  L2 is flushed (256 MiB write) before every timed step, outside the step's 
 
 The same line carries, under "sub_records", one fully measured record (its own step time,
 roofline of the dominant kernel, e2e and clocks, timed in the same process) for each other
-workload of the block: prefill B=1 x T=16, B=1 x T=2048, B=4 x T=8192 and the decode step
-of B=64 sequences at position 4095.
+workload of the block: prefill B=1 x T=16, B=1 x T=2048, B=4 x T=8192, the decode step of
+B=64 sequences at position 4095, and a chunked prefill (the last 2048 tokens of a
+32768-token prompt against a cache of the first 30720).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--no-sub]
                   [--impl reference]
@@ -618,7 +619,8 @@ def measure_gpu(args, w: gin.Workload, inp, world, rank, local, steps, warmup):
 
 
 HEADLINE = "prefill_b1_t32768"
-SUB_WORKLOADS = ("prefill_b1_t16", "prefill_b1_t2048", "prefill_b4_t8192", "decode_b64_pos4095")
+SUB_WORKLOADS = ("prefill_b1_t16", "prefill_b1_t2048", "prefill_b4_t8192", "decode_b64_pos4095",
+                 "prefill_b1_t2048_pos30720")
 # Short steps are timed over at least this many steps so that one record spans a few ms.
 MIN_SUB_STEPS = 100
 
